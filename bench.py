@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused feed-forward block on GB300, one JSON line on stdout.
+
+Step = one forward of the GeGLU feed-forward block at 70B-class size
+(T=8192 tokens, D=8192, H=28672: gate+up dual GEMM with the gelu_tanh(g)*u epilogue, then
+the down GEMM) through the C ABI, inputs resident in HBM. The weights (1.41 GB) are far
+larger than L2, so every step streams them from HBM again. Extra keys report the other
+workloads (GPT-2-small GeGLU, the 4096-wide MLP at 4096 tokens and at 1 token, the small
+fused block, the single Linear), the dominant kernel's roofline, an end-to-end number with
+host buffers, and the oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torch.distributed.run: every rank runs its own replica of the step on its
+own GPU (weak scaling, no collective in the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MLP fwd TFLOP/s & % BF16 peak; batch-1 latency µs & % HBM GB/s"
+HEADLINE = "geglu_8192x8192x28672"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-extras", action="store_true", help="headline only")
+    p.add_argument("--cpu-sample-rows", type=int, default=0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------- distributed
+
+class Dist:
+    def __init__(self, n):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world != n and n > 1:
+            raise SystemExit(f"--gpus {n} but WORLD_SIZE={self.world}: launch with torchrun")
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float, device=None) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------- our arm
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import feed_forward_gemm_gb300 as fm
+    import synth
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    dist.init("nccl")
+    fm.load()
+    stream = torch.cuda.current_stream(dev)
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def events_time(fn, iters):
+        """ms per iteration of fn() over `iters` calls, CUDA events on the launching stream."""
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(iters):
+            fn()
+        end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end) / iters
+
+    # ---------------- headline workload: inputs resident in HBM
+    w = synth.WORKLOADS[HEADLINE]
+    t = w.generate()
+    x, Wg, Wu, Wd = up(t["x"]), up(t["Wg"]), up(t["Wu"]), up(t["Wd"])
+    y = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    ws_bytes = fm.fmlp_geglu_workspace_size(w.T, w.D, w.H)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    m = ws.view(torch.bfloat16).view(w.T, w.H)
+
+    def step():
+        fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, ws_bytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fm.fmlp_device_status(stream) != fm.FMLP_OK:
+        raise SystemExit(f"device status after warm-up: {fm.fmlp_last_error()}")
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    ms = events_time(step, args.steps)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    ms_max = dist.max(ms, dev)
+    flops = w.flops()
+    value = dist.world * flops / (ms_max * 1e-3) / 1e12
+
+    # ---------------- dominant kernel alone: gate+up dual GEMM with the GeGLU epilogue
+    gu_flops = 2 * 2 * w.T * w.D * w.H
+    for _ in range(2):
+        fm.fmlp_geglu_gate_up(x, Wg, Wu, m, w.T, w.D, w.H, stream)
+    gu_ms = events_time(lambda: fm.fmlp_geglu_gate_up(x, Wg, Wu, m, w.T, w.D, w.H, stream),
+                        max(3, args.steps))
+    down_ms = events_time(lambda: fm.fmlp_linear_bias(m, Wd, None, y, w.T, w.H, w.D, stream),
+                          max(3, args.steps))
+    pk, pk_src = peaks()
+    gu_tflops = gu_flops / (gu_ms * 1e-3) / 1e12
+    roofline = {
+        "kernel": "gemm_tc_kernel<256, EPI_GEGLU> (gate+up dual GEMM, gelu_tanh(g)*u epilogue)",
+        "bound": "tensor", "achieved": round(gu_tflops, 1), "peak": pk["bf16_tflops"],
+        "unit": "TFLOP/s", "frac": round(gu_tflops / pk["bf16_tflops"], 4),
+        "peak_source": f"{pk_src} bf16 burst (kernel timed alone)",
+        "traffic": traffic_for("gemm_tc_geglu", gu_flops),
+        "algorithmic_flops_per_launch": gu_flops, "ms_per_launch": round(gu_ms, 4),
+        "down_gemm": {"ms_per_launch": round(down_ms, 4),
+                      "tflops": round(2 * w.T * w.D * w.H / (down_ms * 1e-3) / 1e12, 1)},
+    }
+    torch.cuda.synchronize(dev)
+    if fm.fmlp_device_status(stream) != fm.FMLP_OK:
+        raise SystemExit(f"device status after timing: {fm.fmlp_last_error()}")
+
+    # ---------------- end to end through the C ABI with host buffers
+    x_host = torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        fm.fmlp_geglu(x_dev, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, ws_bytes, stream)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_iters = max(3, args.steps // 2)
+    dist.barrier()
+    t0 = time.perf_counter()
+    e2e_ms = events_time(e2e_step, e2e_iters)
+    wall_ms = (time.perf_counter() - t0) * 1e3 / e2e_iters
+    e2e_ms = dist.max(max(e2e_ms, wall_ms), dev)
+    e2e = {"value": round(dist.world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+           "ms_per_step": round(e2e_ms, 4)}
+    del x_host, y_host, x_dev
+
+    extras = {}
+    if not args.no_extras:
+        extras = run_extras(fm, synth, torch, np, dev, stream, events_time, pk)
+    del x, Wg, Wu, Wd, y, ws
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if dist.rank == 0:
+        cpu = cpu_baseline(t, w, args.cpu_sample_rows)
+
+    launches_per_step = 2
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller; x~N(0,1), W~U(+-1/sqrt(in)))",
+        "config": {"workload": f"{HEADLINE}: GeGLU FFN T=8192 D=8192 H=28672, bias-free, "
+                               "gelu_tanh, bf16 in / fp32 acc / bf16 out",
+                   "T": w.T, "D": w.D, "H": w.H, "flops_per_step": flops,
+                   "l2": "inputs larger than L2 (1.41 GB of weights streamed per step)",
+                   "parallelism": f"replicas x{dist.world} (one block per GPU, no collective)"},
+        "roofline": roofline,
+        "pct_bf16_peak": round(value / dist.world / pk["bf16_tflops_sustained"], 4),
+        "pct_bf16_peak_basis": f"{pk_src} sustained bf16 (whole step is seconds-long loop)",
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "workloads": extras,
+    }
+    dist.barrier()
+    dist.close()
+    return out
+
+
+def traffic_for(name: str, units):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[name]
+        from feed_forward_gemm_gb300 import _build
+        if e.get("source_fingerprint") != _build.kernel_fingerprint():
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
+    """The other workloads, each timed alone with CUDA events (device-resident inputs)."""
+    out = {}
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # GPT-2-small-shaped GeGLU FFN
+    w = synth.WORKLOADS["geglu_8192x768x3072"]
+    t = w.generate()
+    x, Wg, Wu, Wd = up(t["x"]), up(t["Wg"]), up(t["Wu"]), up(t["Wd"])
+    y = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    wsb = fm.fmlp_geglu_workspace_size(w.T, w.D, w.H)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def geglu4():
+        flush.zero_()   # evict L2 (256 MB > 129 MB) so weights come from HBM
+
+    fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream)
+    t_flush = events_time(geglu4, 10)
+    t_all = events_time(lambda: (geglu4(), fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws,
+                                                         wsb, stream)), 20)
+    ms = max(t_all - t_flush, 1e-6)
+    out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
+                   "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                   "l2": "flushed between iterations (256 MB write), flush time subtracted"}
+    del x, Wg, Wu, Wd, y, ws
+
+    # 4096-wide Linear -> GELU(erf) -> Linear with biases at 4096 tokens
+    w = synth.WORKLOADS["mlp_4096_t4096"]
+    t = w.generate()
+    d = {k: up(v) for k, v in t.items()}
+    y = torch.empty((w.T, w.Dout), dtype=torch.bfloat16, device=dev)
+    wsb = fm.fmlp_mlp_gelu_workspace_size(w.T, w.D, w.H, w.Dout)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+
+    def mlp():
+        fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, w.T, w.D, w.H, w.Dout,
+                         fm.FMLP_GELU_ERF, ws, wsb, stream)
+    mlp()
+    t_all = events_time(lambda: (geglu4(), mlp()), 20)
+    ms = max(t_all - t_flush, 1e-6)
+    out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
+                   "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                   "l2": "flushed between iterations, flush time subtracted"}
+    del d, y, ws
+
+    # the same MLP at one token (decode): weights rotate through 5 copies (320 MB > 2x L2)
+    w = synth.WORKLOADS["mlp_4096_t1"]
+    sets = []
+    for r in range(5):
+        t = w.generate(replica=r)
+        sets.append({k: up(v) for k, v in t.items()})
+    y = torch.empty((1, w.Dout), dtype=torch.bfloat16, device=dev)
+    wsb = fm.fmlp_mlp_gelu_workspace_size(1, w.D, w.H, w.Dout)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    ctr = [0]
+
+    def dec():
+        s = sets[ctr[0] % 5]
+        ctr[0] += 1
+        fm.fmlp_mlp_gelu(s["x"], s["W1"], s["b1"], s["W2"], s["b2"], y, 1, w.D, w.H, w.Dout,
+                         fm.FMLP_GELU_ERF, ws, wsb, stream)
+    for _ in range(10):
+        dec()
+    ms = events_time(dec, 200)
+    wbytes = 2 * (w.D * w.H + w.H * w.Dout)
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    out[w.name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
+                   "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                   "plan": fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout),
+                   "l2": "5 rotating weight sets (336 MB)"}
+    s0 = sets[0]
+    sets.clear()
+    del s0, y, ws
+
+    # small fully fused GeGLU block and the single Linear: launch-latency bound
+    for name in ("geglu_1024x32x64", "linear_1024x32x64"):
+        w = synth.WORKLOADS[name]
+        t = w.generate()
+        d = {k: up(v) for k, v in t.items()}
+        if w.op == "geglu":
+            y = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+            wsb = fm.fmlp_geglu_workspace_size(w.T, w.D, w.H)
+            ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+            fn = (lambda: fm.fmlp_geglu(d["x"], d["Wg"], d["Wu"], d["Wd"], y, w.T, w.D, w.H, ws,
+                                        wsb, stream))
+        else:
+            y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+            fn = lambda: fm.fmlp_linear_bias(d["x"], d["W"], d["b"], y, w.T, w.D, w.H, stream)
+        for _ in range(10):
+            fn()
+        ms = events_time(fn, 200)
+        out[name] = {"us": round(ms * 1e3, 2), "bound": "launch latency"}
+    return out
+
+
+# ------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(t, w, rows_req: int):
+    """The oracle on a bounded sample of the headline workload's token rows."""
+    import numpy as np
+
+    import oracle
+    nthreads = oracle.threads()
+    rows_n = rows_req or max(2, min(64, nthreads))
+    rows = np.arange(rows_n, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"], rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    flops = w.flops() * rows_n / w.T
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": min(nthreads, rows_n),
+            "kind": "oracle",
+            "sample": f"{rows_n} of {w.T} token rows of {w.name} (full H), fp64 C oracle, "
+                      f"{dt:.2f} s; flops scaled to the rows computed"}
+
+
+# ------------------------------------------------------------------------- reference arm
+
+def run_reference(args, dist: Dist):
+    """The oracle (the plain fp64 CPU implementation) as the reference arm: each step is a
+    bounded sample of the headline workload's rows."""
+    if dist.rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    import synth
+    w = synth.WORKLOADS[HEADLINE]
+    t = w.generate()
+    nthreads = oracle.threads()
+    rows_n = max(2, min(16, nthreads))
+    for i in range(args.warmup):
+        oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"], rows=np.arange(1, dtype=np.int64),
+                     nthreads=1)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        rows = (np.arange(rows_n, dtype=np.int64) + s * rows_n) % w.T
+        oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"], rows=rows, nthreads=nthreads)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = w.flops() * rows_n / w.T
+    value = flops / dt / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{HEADLINE} (oracle on {rows_n} token rows per step)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                         "cores": min(nthreads, rows_n), "kind": "oracle",
+                         "sample": f"{rows_n} of {w.T} token rows per step, full H"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    if args.impl == "reference":
+        out = run_reference(args, dist)
+    else:
+        out = run_ours(args, dist)
+    if out is not None and dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

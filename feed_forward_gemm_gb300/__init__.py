@@ -1,0 +1,214 @@
+"""Python binding of the fmlp C ABI (include/fmlp.h): argument marshalling only.
+
+Every entry point here has the C name and forwards plain device pointers and sizes to the
+shared library built from csrc/. No computation happens in Python: if the library is
+missing the import of a function fails loudly (there is no fallback of any kind).
+
+Tensors may be passed as torch tensors (their data_ptr() is used; they must be contiguous
+CUDA tensors of the documented shape) or as raw integer device addresses. `stream` may be a
+torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "FmlpError", "load", "build", "library_path",
+    "fmlp_linear_bias", "fmlp_linear_bias_gelu", "fmlp_geglu_gate_up", "fmlp_geglu",
+    "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
+    "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
+    "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
+    "fmlp_version",
+    "FMLP_OK", "FMLP_ERR_NULL", "FMLP_ERR_SHAPE", "FMLP_ERR_ALIGN", "FMLP_ERR_ALIAS",
+    "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
+    "FMLP_GELU_TANH", "FMLP_GELU_ERF", "FMLP_PLAN_NONE", "FMLP_PLAN_TC",
+    "FMLP_PLAN_FUSED_SMALL", "FMLP_PLAN_GEMV",
+]
+
+FMLP_OK, FMLP_ERR_NULL, FMLP_ERR_SHAPE, FMLP_ERR_ALIGN, FMLP_ERR_ALIAS = 0, 1, 2, 3, 4
+FMLP_ERR_WORKSPACE, FMLP_ERR_CUDA, FMLP_ERR_DEVICE_TIMEOUT, FMLP_ERR_DEVICE = 5, 6, 7, 8
+FMLP_GELU_TANH, FMLP_GELU_ERF = 0, 1
+FMLP_PLAN_NONE, FMLP_PLAN_TC, FMLP_PLAN_FUSED_SMALL, FMLP_PLAN_GEMV = 0, 1, 2, 3
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_INT = ctypes.c_int
+
+# name -> (restype, argtypes); the order matches include/fmlp.h
+_SIGNATURES = {
+    "fmlp_linear_bias": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fmlp_linear_bias_gelu": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P]),
+    "fmlp_geglu_gate_up": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fmlp_geglu": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "fmlp_mlp_gelu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _INT, _P, _SZ, _P]),
+    "fmlp_geglu_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "fmlp_mlp_gelu_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+    "fmlp_geglu_plan": (_INT, [_I64, _I64, _I64]),
+    "fmlp_mlp_gelu_plan": (_INT, [_I64, _I64, _I64, _I64]),
+    "fmlp_linear_plan": (_INT, [_I64, _I64, _I64]),
+    "fmlp_gelu_eval": (_INT, [_P, _P, _I64, _INT, _P]),
+    "fmlp_device_status": (_INT, [_P]),
+    "fmlp_test_wait_timeout": (_INT, [_I64, _P]),
+    "fmlp_status_string": (ctypes.c_char_p, [_INT]),
+    "fmlp_last_error": (ctypes.c_char_p, []),
+    "fmlp_version": (_INT, []),
+}
+
+
+class FmlpError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where} -> status {status} ({_status_text(status)}): {detail}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def load(build_if_missing: bool = False):
+    """Load the shared library (raising if it is absent and build_if_missing is False)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise ImportError(
+                    f"fmlp CUDA library not built ({path} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _status_text(st: int) -> str:
+    try:
+        return load().fmlp_status_string(st).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        if hasattr(t, "is_contiguous") and not t.is_contiguous():
+            raise ValueError("fmlp tensors must be contiguous")
+        return t.data_ptr() or None
+    raise TypeError(f"cannot take a device pointer from {type(t)!r}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream or None
+    raise TypeError(f"cannot take a CUDA stream from {type(s)!r}")
+
+
+def _check(st: int, where: str, raise_on_error: bool):
+    if st != FMLP_OK and raise_on_error:
+        raise FmlpError(st, where, fmlp_last_error())
+    return st
+
+
+def fmlp_status_string(st: int) -> str:
+    return load().fmlp_status_string(int(st)).decode()
+
+
+def fmlp_last_error() -> str:
+    return load().fmlp_last_error().decode()
+
+
+def fmlp_version() -> int:
+    return int(load().fmlp_version())
+
+
+def fmlp_linear_bias(x, W, b, y, T, in_dim, out_dim, stream=None, raise_on_error=True):
+    st = load().fmlp_linear_bias(_ptr(x), _ptr(W), _ptr(b), _ptr(y), T, in_dim, out_dim,
+                                 _stream(stream))
+    return _check(st, "fmlp_linear_bias", raise_on_error)
+
+
+def fmlp_linear_bias_gelu(x, W, b, h, T, in_dim, out_dim, mode=FMLP_GELU_TANH, stream=None,
+                          raise_on_error=True):
+    st = load().fmlp_linear_bias_gelu(_ptr(x), _ptr(W), _ptr(b), _ptr(h), T, in_dim, out_dim,
+                                      int(mode), _stream(stream))
+    return _check(st, "fmlp_linear_bias_gelu", raise_on_error)
+
+
+def fmlp_geglu_gate_up(x, Wg, Wu, m, T, D, H, stream=None, raise_on_error=True):
+    st = load().fmlp_geglu_gate_up(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(m), T, D, H,
+                                   _stream(stream))
+    return _check(st, "fmlp_geglu_gate_up", raise_on_error)
+
+
+def fmlp_geglu(x, Wg, Wu, Wd, y, T, D, H, ws=None, ws_bytes=0, stream=None,
+               raise_on_error=True):
+    st = load().fmlp_geglu(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(y), T, D, H, _ptr(ws),
+                           int(ws_bytes), _stream(stream))
+    return _check(st, "fmlp_geglu", raise_on_error)
+
+
+def fmlp_mlp_gelu(x, W1, b1, W2, b2, y, T, D, H, Dout, mode=FMLP_GELU_ERF, ws=None, ws_bytes=0,
+                  stream=None, raise_on_error=True):
+    st = load().fmlp_mlp_gelu(_ptr(x), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(y), T, D, H,
+                              Dout, int(mode), _ptr(ws), int(ws_bytes), _stream(stream))
+    return _check(st, "fmlp_mlp_gelu", raise_on_error)
+
+
+def fmlp_geglu_workspace_size(T, D, H) -> int:
+    return int(load().fmlp_geglu_workspace_size(T, D, H))
+
+
+def fmlp_mlp_gelu_workspace_size(T, D, H, Dout) -> int:
+    return int(load().fmlp_mlp_gelu_workspace_size(T, D, H, Dout))
+
+
+def fmlp_geglu_plan(T, D, H) -> int:
+    return int(load().fmlp_geglu_plan(T, D, H))
+
+
+def fmlp_mlp_gelu_plan(T, D, H, Dout) -> int:
+    return int(load().fmlp_mlp_gelu_plan(T, D, H, Dout))
+
+
+def fmlp_linear_plan(T, in_dim, out_dim) -> int:
+    return int(load().fmlp_linear_plan(T, in_dim, out_dim))
+
+
+def fmlp_gelu_eval(x, out, n, mode=FMLP_GELU_TANH, stream=None, raise_on_error=True):
+    st = load().fmlp_gelu_eval(_ptr(x), _ptr(out), n, int(mode), _stream(stream))
+    return _check(st, "fmlp_gelu_eval", raise_on_error)
+
+
+def fmlp_device_status(stream=None) -> int:
+    return int(load().fmlp_device_status(_stream(stream)))
+
+
+def fmlp_test_wait_timeout(timeout_us, stream=None, raise_on_error=True):
+    st = load().fmlp_test_wait_timeout(int(timeout_us), _stream(stream))
+    return _check(st, "fmlp_test_wait_timeout", raise_on_error)

@@ -1,0 +1,37 @@
+// Device activations shared by every epilogue.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace fmlp {
+
+// GELU, tanh form: 0.5 x (1 + tanh(z)), z = sqrt(2/pi) (x + 0.044715 x^3).
+// Evaluated through the identity (1 + tanh z) / 2 = 1 / (1 + e^{-2z}), so one fast exponential
+// and one fast divide replace tanh. As x -> -inf the exponential overflows to +inf and the
+// quotient goes to 0 (the correct limit); as x -> +inf it returns x.
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float two_k = 1.5957691216057308f;          // 2 * sqrt(2 / pi)
+  const float z2 = two_k * x * fmaf(0.044715f * x, x, 1.0f);
+  return __fdividef(x, 1.0f + __expf(-z2));
+}
+
+// GELU, exact: 0.5 x (1 + erf(x / sqrt 2)).
+__device__ __forceinline__ float gelu_erf_f(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ float gelu_f(float x, int mode) {
+  return mode == 1 ? gelu_erf_f(x) : gelu_tanh_f(x);
+}
+
+// Two floats -> packed bf16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace fmlp

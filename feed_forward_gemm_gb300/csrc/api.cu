@@ -1,0 +1,530 @@
+// Host side of the C ABI declared in include/fmlp.h: argument validation, plan choice,
+// tensor-map encoding and launches on the caller's stream.
+//
+// Dispatch follows the lesson of "Profiling in PyTorch (Part 2): From nn.Linear to a Fused
+// MLP" (sections "Stacking three Linears: the MLP" and "Why tuned kernels are better"): no
+// per-call occupancy query (the SM count is cached once per device), one shape-generic binary
+// whose tile shape is picked at run time from a small cost model, no recompilation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fmlp.h"
+#include "internal.h"
+
+namespace fmlp {
+
+// Per-device status word written by kernels that give up on a bounded wait.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per wait
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647;
+
+thread_local std::string t_last_error;
+
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fmlp_status cuda_fail(cudaError_t e, const char* what) {
+  set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return FMLP_ERR_CUDA;
+}
+
+// Current device's cached state; checks the architecture once.
+fmlp_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d out of range", dev);
+    return FMLP_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+        cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+        cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if (d.major != 10 || d.minor != 3) {
+      set_error("device %d is compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                dev, d.major, d.minor);
+      return FMLP_ERR_DEVICE;
+    }
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        set_error("cuTensorMapEncodeTiled unavailable from the driver");
+        return FMLP_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return FMLP_OK;
+}
+
+// Row-major bf16 matrix [rows, cols] -> 2-D tensor map with a {64, box_rows} box, 128B swizzle.
+fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                     uint32_t box_rows, const char* name) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2u};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(%s [%lld x %lld], box %u rows) failed with CUresult %d",
+              name, static_cast<long long>(rows), static_cast<long long>(cols), box_rows,
+              static_cast<int>(r));
+    return FMLP_ERR_CUDA;
+  }
+  return FMLP_OK;
+}
+
+// ------------------------------------------------------------------------- validation
+
+struct Range {
+  const void* p;
+  size_t bytes;
+  const char* name;
+};
+
+bool overlaps(const Range& a, const Range& b) {
+  if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+fmlp_status check_T(int64_t T) {
+  if (T < 0 || T > kMaxDim) {
+    set_error("T = %lld is out of range [0, 2^31-1]", static_cast<long long>(T));
+    return FMLP_ERR_SHAPE;
+  }
+  return FMLP_OK;
+}
+
+fmlp_status check_inner(int64_t v, const char* name) {
+  if (v < 1 || v > kMaxDim || (v % 8) != 0) {
+    set_error("%s = %lld must be in [8, 2^31-1] and a multiple of 8", name,
+              static_cast<long long>(v));
+    return FMLP_ERR_SHAPE;
+  }
+  return FMLP_OK;
+}
+
+fmlp_status check_ptrs(const Range* r, int n, bool nullable_mask_last = false) {
+  (void)nullable_mask_last;
+  for (int i = 0; i < n; ++i) {
+    if (!r[i].p) continue;
+    if (reinterpret_cast<uintptr_t>(r[i].p) % 16 != 0) {
+      set_error("%s is not 16-byte aligned", r[i].name);
+      return FMLP_ERR_ALIGN;
+    }
+  }
+  return FMLP_OK;
+}
+
+fmlp_status check_alias(const Range& out, const Range* in, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (overlaps(out, in[i])) {
+      set_error("%s overlaps %s", out.name, in[i].name);
+      return FMLP_ERR_ALIAS;
+    }
+  }
+  return FMLP_OK;
+}
+
+#define FMLP_TRY(expr)                 \
+  do {                                 \
+    fmlp_status _st = (expr);          \
+    if (_st != FMLP_OK) return _st;    \
+  } while (0)
+
+#define FMLP_NONNULL(p, name)                         \
+  do {                                                \
+    if (!(p)) {                                       \
+      set_error("%s is NULL", name);                  \
+      return FMLP_ERR_NULL;                           \
+    }                                                 \
+  } while (0)
+
+size_t mat_bytes(int64_t r, int64_t c) { return static_cast<size_t>(r) * static_cast<size_t>(c) * 2u; }
+
+// ------------------------------------------------------------------------- tile choice
+
+// Persistent grid: each CTA takes tiles round-robin, so the critical path is
+// ceil(tiles / SMs) tiles of work proportional to bn. Narrow tiles cost extra shared-memory
+// bandwidth per FLOP; the efficiency factors reflect that.
+int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu) {
+  const int cands[3] = {64, 128, 256};
+  const double eff[3] = {0.60, 0.85, 1.0};
+  int best = 0;
+  double best_cost = 1e300;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = cands[i];
+    if (geglu && bn < 128) continue;
+    const int bn_out = geglu ? bn / 2 : bn;
+    const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * bn / eff[i];
+    // candidates come in increasing bn; a (near) tie goes to the wider tile
+    if (best == 0 || cost <= best_cost * 1.001) {
+      best = bn;
+      best_cost = std::min(best_cost, cost);
+    }
+  }
+  return best;
+}
+
+fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
+                        const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
+                        int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
+  GemmLaunch L;
+  memset(&L, 0, sizeof L);
+  const bool geglu = epi == EPI_GEGLU;
+  L.bn = pick_bn(M, N_out, d.sms, geglu);
+  const uint32_t b_rows = geglu ? L.bn / 2 : L.bn;
+  FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A"));
+  FMLP_TRY(make_map(&L.tmB0, B0, N_out, K, b_rows, "B"));
+  if (geglu) {
+    FMLP_TRY(make_map(&L.tmB1, B1, N_out, K, b_rows, "B_up"));
+  } else {
+    L.tmB1 = L.tmB0;
+  }
+  FMLP_TRY(make_map(&L.tmY, Y, M, N_out, 32, "Y"));
+  L.bias = bias;
+  L.M = static_cast<int>(M);
+  L.N_out = static_cast<int>(N_out);
+  L.K = static_cast<int>(K);
+  L.gelu_mode = gelu_mode;
+  L.epi = epi;
+  const int bn_out = geglu ? L.bn / 2 : L.bn;
+  const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
+  L.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
+  L.pdl = pdl;
+  L.stream = s;
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
+  cudaError_t e = gemm_tc_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_tc launch");
+  return FMLP_OK;
+}
+
+}  // namespace
+}  // namespace fmlp
+
+using namespace fmlp;
+
+extern "C" {
+
+int fmlp_version(void) { return 100; }
+
+const char* fmlp_status_string(fmlp_status st) {
+  switch (st) {
+    case FMLP_OK: return "FMLP_OK";
+    case FMLP_ERR_NULL: return "FMLP_ERR_NULL: a required pointer is NULL";
+    case FMLP_ERR_SHAPE: return "FMLP_ERR_SHAPE: invalid dimension";
+    case FMLP_ERR_ALIGN: return "FMLP_ERR_ALIGN: pointer not 16-byte aligned";
+    case FMLP_ERR_ALIAS: return "FMLP_ERR_ALIAS: output overlaps an input";
+    case FMLP_ERR_WORKSPACE: return "FMLP_ERR_WORKSPACE: workspace too small";
+    case FMLP_ERR_CUDA: return "FMLP_ERR_CUDA: CUDA call failed";
+    case FMLP_ERR_DEVICE_TIMEOUT: return "FMLP_ERR_DEVICE_TIMEOUT: a device wait ran out";
+    case FMLP_ERR_DEVICE: return "FMLP_ERR_DEVICE: unsupported device";
+    default: return "unknown fmlp_status";
+  }
+}
+
+const char* fmlp_last_error(void) { return t_last_error.c_str(); }
+
+size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
+  (void)D;
+  if (T <= 0 || H <= 0) return 0;
+  return mat_bytes(T, H);
+}
+
+size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout) {
+  (void)D;
+  (void)Dout;
+  if (T <= 0 || H <= 0) return 0;
+  return mat_bytes(T, H);
+}
+
+int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) {
+  (void)D;
+  (void)H;
+  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
+}
+
+int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout) {
+  (void)D;
+  (void)H;
+  (void)Dout;
+  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
+}
+
+int fmlp_linear_plan(int64_t T, int64_t in, int64_t out) {
+  (void)in;
+  (void)out;
+  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
+}
+
+static fmlp_status linear_common(const void* x, const void* W, const void* b, void* y,
+                                 int64_t T, int64_t in, int64_t out, int epi, int mode,
+                                 fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(in, "in"));
+  FMLP_TRY(check_inner(out, "out"));
+  if (epi == EPI_BIAS_GELU && mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
+    set_error("gelu mode %d is not FMLP_GELU_TANH or FMLP_GELU_ERF", mode);
+    return FMLP_ERR_SHAPE;
+  }
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(W, "W");
+  FMLP_NONNULL(y, "y");
+  const Range rx{x, mat_bytes(T, in), "x"}, rw{W, mat_bytes(out, in), "W"},
+      rb{b, b ? mat_bytes(1, out) : 0, "b"}, ry{y, mat_bytes(T, out), "y"};
+  const Range ins[3] = {rx, rw, rb};
+  const Range all[4] = {rx, rw, rb, ry};
+  FMLP_TRY(check_ptrs(all, 4));
+  FMLP_TRY(check_alias(ry, ins, 3));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  return launch_gemm(*d, epi, x, W, nullptr, b, y, T, out, in, mode, false,
+                     reinterpret_cast<cudaStream_t>(s));
+}
+
+fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y, int64_t T,
+                             int64_t in, int64_t out, fmlp_stream_t s) {
+  return linear_common(x, W, b, y, T, in, out, EPI_BIAS, 0, s);
+}
+
+fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,
+                                  int64_t T, int64_t in, int64_t out, fmlp_gelu_mode mode,
+                                  fmlp_stream_t s) {
+  return linear_common(x, W, b, h, T, in, out, EPI_BIAS_GELU, static_cast<int>(mode), s);
+}
+
+fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, void* m, int64_t T,
+                               int64_t D, int64_t H, fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(D, "D"));
+  FMLP_TRY(check_inner(H, "H"));
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(Wg, "Wg");
+  FMLP_NONNULL(Wu, "Wu");
+  FMLP_NONNULL(m, "m");
+  const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, mat_bytes(H, D), "Wg"},
+      ru{Wu, mat_bytes(H, D), "Wu"}, rm{m, mat_bytes(T, H), "m"};
+  const Range ins[3] = {rx, rg, ru};
+  const Range all[4] = {rx, rg, ru, rm};
+  FMLP_TRY(check_ptrs(all, 4));
+  FMLP_TRY(check_alias(rm, ins, 3));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  return launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false,
+                     reinterpret_cast<cudaStream_t>(s));
+}
+
+fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
+                       int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
+                       fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(D, "D"));
+  FMLP_TRY(check_inner(H, "H"));
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(Wg, "Wg");
+  FMLP_NONNULL(Wu, "Wu");
+  FMLP_NONNULL(Wd, "Wd");
+  FMLP_NONNULL(y, "y");
+  const size_t need = fmlp_geglu_workspace_size(T, D, H);
+  if (ws && ws_bytes < need) {
+    set_error("workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return FMLP_ERR_WORKSPACE;
+  }
+  const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, mat_bytes(H, D), "Wg"},
+      ru{Wu, mat_bytes(H, D), "Wu"}, rd{Wd, mat_bytes(D, H), "Wd"}, ry{y, mat_bytes(T, D), "y"},
+      rw{ws, ws ? need : 0, "workspace"};
+  const Range all[6] = {rx, rg, ru, rd, ry, rw};
+  FMLP_TRY(check_ptrs(all, 6));
+  const Range ins_y[5] = {rx, rg, ru, rd, rw};
+  FMLP_TRY(check_alias(ry, ins_y, 5));
+  const Range ins_w[4] = {rx, rg, ru, rd};
+  FMLP_TRY(check_alias(rw, ins_w, 4));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  void* m = ws;
+  if (!m) {
+    cudaError_t e = cudaMallocAsync(&m, need, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+  }
+  fmlp_status r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
+  if (r == FMLP_OK) r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st);
+  if (!ws) {
+    cudaError_t e = cudaFreeAsync(m, st);
+    if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
+  }
+  return r;
+}
+
+fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const void* W2,
+                          const void* b2, void* y, int64_t T, int64_t D, int64_t H, int64_t Dout,
+                          fmlp_gelu_mode mode, void* ws, size_t ws_bytes, fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(D, "D"));
+  FMLP_TRY(check_inner(H, "H"));
+  FMLP_TRY(check_inner(Dout, "Dout"));
+  if (mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
+    set_error("gelu mode %d is not FMLP_GELU_TANH or FMLP_GELU_ERF", static_cast<int>(mode));
+    return FMLP_ERR_SHAPE;
+  }
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(W1, "W1");
+  FMLP_NONNULL(W2, "W2");
+  FMLP_NONNULL(y, "y");
+  const size_t need = fmlp_mlp_gelu_workspace_size(T, D, H, Dout);
+  if (ws && ws_bytes < need) {
+    set_error("workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return FMLP_ERR_WORKSPACE;
+  }
+  const Range rx{x, mat_bytes(T, D), "x"}, r1{W1, mat_bytes(H, D), "W1"},
+      rb1{b1, b1 ? mat_bytes(1, H) : 0, "b1"}, r2{W2, mat_bytes(Dout, H), "W2"},
+      rb2{b2, b2 ? mat_bytes(1, Dout) : 0, "b2"}, ry{y, mat_bytes(T, Dout), "y"},
+      rw{ws, ws ? need : 0, "workspace"};
+  const Range all[7] = {rx, r1, rb1, r2, rb2, ry, rw};
+  FMLP_TRY(check_ptrs(all, 7));
+  const Range ins_y[6] = {rx, r1, rb1, r2, rb2, rw};
+  FMLP_TRY(check_alias(ry, ins_y, 6));
+  const Range ins_w[5] = {rx, r1, rb1, r2, rb2};
+  FMLP_TRY(check_alias(rw, ins_w, 5));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  void* h = ws;
+  if (!h) {
+    cudaError_t e = cudaMallocAsync(&h, need, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+  }
+  fmlp_status r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D,
+                              static_cast<int>(mode), false, st);
+  if (r == FMLP_OK) r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st);
+  if (!ws) {
+    cudaError_t e = cudaFreeAsync(h, st);
+    if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
+  }
+  return r;
+}
+
+fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,
+                           fmlp_stream_t s) {
+  t_last_error.clear();
+  if (n < 0) {
+    set_error("n = %lld < 0", static_cast<long long>(n));
+    return FMLP_ERR_SHAPE;
+  }
+  if (mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
+    set_error("gelu mode %d invalid", static_cast<int>(mode));
+    return FMLP_ERR_SHAPE;
+  }
+  if (n == 0) return FMLP_OK;
+  FMLP_NONNULL(in, "in");
+  FMLP_NONNULL(out, "out");
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaError_t e = gelu_eval_launch(in, out, n, static_cast<int>(mode),
+                                   reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "gelu_eval launch");
+  return FMLP_OK;
+}
+
+fmlp_status fmlp_device_status(fmlp_stream_t s) {
+  t_last_error.clear();
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read device status");
+  if (v == 0) return FMLP_OK;
+  const int zero = 0;
+  if ((e = cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "clear device status");
+  static const char* sites[] = {"?",          "test wait",          "producer (empty slot)",
+                                "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
+                                "drain",      "fused kernel"};
+  const int site = v >> 8;
+  set_error("a kernel gave up waiting at: %s (code 0x%x)",
+            (site >= 0 && site < 8) ? sites[site] : "?", v);
+  return static_cast<fmlp_status>(v & 0xFF);
+}
+
+fmlp_status fmlp_test_wait_timeout(int64_t timeout_us, fmlp_stream_t s) {
+  t_last_error.clear();
+  if (timeout_us < 1 || timeout_us > 2000000) {
+    set_error("timeout_us = %lld out of range [1, 2000000]", static_cast<long long>(timeout_us));
+    return FMLP_ERR_SHAPE;
+  }
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaError_t e = wait_timeout_launch(static_cast<uint64_t>(timeout_us) * 1000u, d->status,
+                                      reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "wait_timeout launch");
+  return FMLP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,164 @@
+/*
+ * fmlp.h - C ABI of the fused transformer feed-forward library for GB300 (sm_103a).
+ *
+ * Operations (all source citations are to "Profiling in PyTorch (Part 2): From nn.Linear to
+ * a Fused MLP" unless another page is named):
+ *   fmlp_linear_bias   y = x @ W^T + b with the bias added in the GEMM epilogue
+ *                      (sections "From matmul-add to Linear" and "Why are there no separate
+ *                      mul and add kernels?"; the weight is read in its stored [out, in]
+ *                      layout, the transpose being only a view, section "Where did the
+ *                      transpose go? Kernel layouts and pre-ops").
+ *   fmlp_geglu         the GeGLU feed-forward block of section "Stacking three Linears: the
+ *                      MLP": g = x Wg^T, u = x Wu^T, m = gelu_tanh(g) * u, y = m Wd^T, with
+ *                      gelu(g)*u fused into the gate/up GEMM epilogue (sections "The fused
+ *                      Triton kernel" and "Why tuned kernels are better" fuse it as a separate
+ *                      pointwise pass; here it never leaves the GEMM).
+ *   fmlp_mlp_gelu      Linear -> GELU -> Linear with biases, y = W2 GELU(W1 x + b1) + b2
+ *                      (ainews.cool fused-MLP article, technical deep-dive and benchmark
+ *                      sections: one launch instead of three at batch 1).
+ *
+ * Common conventions
+ *   - Tensors are dense, row-major (last index fastest), contiguous, bfloat16 bit patterns in
+ *     device memory. x is [T, in]; weights use the nn.Linear layout [out, in]; biases [out].
+ *     T is the token count batch*seq (section "Why are there two kinds of GEMM kernels?").
+ *   - Accumulation is fp32. The bias is added in fp32 before the activation. The output and
+ *     the one intermediate (m or h) are each rounded to bf16 once, round-to-nearest-even.
+ *   - Every call is asynchronous on the caller's stream `s` (NULL = legacy default stream)
+ *     and launches only hand-written kernels. Results are valid once `s` has synchronised.
+ *     Results are deterministic: no atomics take part in any sum.
+ *   - Ownership: all tensor and workspace pointers belong to the caller; the library keeps
+ *     none of them after the call returns. The library owns only per-device caches (SM count,
+ *     CUDA function attributes, encoded tensor maps), guarded by a mutex; the calls are
+ *     thread-safe.
+ *   - Requirements checked before anything is launched (the status names the first failure):
+ *       FMLP_ERR_NULL       a required pointer is NULL
+ *       FMLP_ERR_SHAPE      T < 0, or an inner dimension (in/out/D/H/Dout) < 1 or not a
+ *                           multiple of 8, or a dimension above 2^31 - 1
+ *       FMLP_ERR_ALIGN      a tensor pointer not 16-byte aligned
+ *       FMLP_ERR_ALIAS      the output overlaps an input (or the workspace)
+ *       FMLP_ERR_WORKSPACE  ws_bytes smaller than the matching *_workspace_size()
+ *       FMLP_ERR_DEVICE     the current device is not compute capability 10.3
+ *     T == 0 returns FMLP_OK and launches nothing. A failed launch returns FMLP_ERR_CUDA with
+ *     the CUDA error text in fmlp_last_error(). The library never aborts the process.
+ *   - Device-side waits are bounded (about one second). A wait that runs out makes the kernel
+ *     record the fault in a per-device status word and return early; the output is then
+ *     undefined and fmlp_device_status() reports FMLP_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef FMLP_H_
+#define FMLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FMLP_API __attribute__((visibility("default")))
+#else
+#define FMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st* fmlp_stream_t;
+
+typedef enum {
+    FMLP_OK = 0,
+    FMLP_ERR_NULL = 1,
+    FMLP_ERR_SHAPE = 2,
+    FMLP_ERR_ALIGN = 3,
+    FMLP_ERR_ALIAS = 4,
+    FMLP_ERR_WORKSPACE = 5,
+    FMLP_ERR_CUDA = 6,
+    FMLP_ERR_DEVICE_TIMEOUT = 7,
+    FMLP_ERR_DEVICE = 8
+} fmlp_status;
+
+/* GELU flavour. TANH: 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))), the
+ * approximate="tanh" form of section "Stacking three Linears: the MLP". ERF: the exact
+ * 0.5 x (1 + erf(x / sqrt 2)), nn.GELU's default. */
+typedef enum { FMLP_GELU_TANH = 0, FMLP_GELU_ERF = 1 } fmlp_gelu_mode;
+
+/* Which kernel sequence a call with these sizes runs (reported by the *_plan queries). */
+typedef enum {
+    FMLP_PLAN_NONE = 0,         /* T == 0: nothing launched */
+    FMLP_PLAN_TC = 1,           /* tcgen05 GEMM kernel(s); GeGLU/MLP: 2 kernels, m/h in ws */
+    FMLP_PLAN_FUSED_SMALL = 2,  /* GeGLU: whole block in 1 kernel, m kept on chip */
+    FMLP_PLAN_GEMV = 3          /* few tokens: weight-streaming GEMV kernel(s) */
+} fmlp_plan;
+
+/* y[T, out] = bf16(x[T, in] @ W[out, in]^T + b[out]).
+ * b may be NULL (no bias). One kernel. Section "Why are there no separate mul and add
+ * kernels?": the bias add is the GEMM's epilogue, done before the write to HBM. */
+FMLP_API fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y,
+                             int64_t T, int64_t in, int64_t out, fmlp_stream_t s);
+
+/* h[T, out] = bf16(GELU(x[T, in] @ W[out, in]^T + b[out])), GELU per `mode`, b nullable.
+ * The first half of fmlp_mlp_gelu as its own call (bias+GELU epilogue). */
+FMLP_API fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,
+                                  int64_t T, int64_t in, int64_t out, fmlp_gelu_mode mode,
+                                  fmlp_stream_t s);
+
+/* m[T, H] = bf16(gelu_tanh(x[T, D] Wg[H, D]^T) * (x Wu[H, D]^T)).
+ * The gate and up GEMMs of one token block run together in one kernel and share the x tile;
+ * gelu(g)*u is the epilogue, so m is written to HBM exactly once. */
+FMLP_API fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, void* m,
+                               int64_t T, int64_t D, int64_t H, fmlp_stream_t s);
+
+/* y[T, D] = bf16(m Wd[D, H]^T) with m = bf16(gelu_tanh(x Wg^T) * (x Wu^T)); bias-free, as in
+ * the page's SimpleGeGLUMLP. ws: device workspace of at least
+ * fmlp_geglu_workspace_size(T, D, H) bytes, 256-byte aligned, that holds m between the two
+ * kernels of the TC plan; NULL with ws_bytes == 0 lets the library take it from the stream-
+ * ordered allocator (cudaMallocAsync/cudaFreeAsync on `s`). */
+FMLP_API fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
+                       int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
+                       fmlp_stream_t s);
+
+/* y[T, Dout] = bf16(h W2[Dout, H]^T + b2) with h = bf16(GELU(x[T, D] W1[H, D]^T + b1)).
+ * b1, b2 nullable. ws as for fmlp_geglu, sized by fmlp_mlp_gelu_workspace_size(). */
+FMLP_API fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const void* W2,
+                          const void* b2, void* y, int64_t T, int64_t D, int64_t H,
+                          int64_t Dout, fmlp_gelu_mode mode, void* ws, size_t ws_bytes,
+                          fmlp_stream_t s);
+
+/* Workspace bytes the calls above need (T*H*2 for the 2-kernel plans, else 0). Pure host
+ * functions; they touch no device. */
+FMLP_API size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H);
+FMLP_API size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout);
+
+/* The plan a call with these sizes takes (an fmlp_plan value). Pure host functions. */
+FMLP_API int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H);
+FMLP_API int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout);
+FMLP_API int fmlp_linear_plan(int64_t T, int64_t in, int64_t out);
+
+/* Device activation check: out[i] = GELU(in[i]) in fp32 with the exact device code the
+ * epilogues use. in/out: n floats in device memory. One kernel. */
+FMLP_API fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,
+                           fmlp_stream_t s);
+
+/* Synchronises `s`, then returns and clears the current device's status word:
+ * FMLP_OK, or FMLP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call (which wait is named in fmlp_last_error()). */
+FMLP_API fmlp_status fmlp_device_status(fmlp_stream_t s);
+
+/* Test hook for the bounded-wait machinery: launches one CTA whose thread waits on an
+ * mbarrier that nothing completes, with a limit of timeout_us microseconds (1..2,000,000).
+ * The kernel then records FMLP_ERR_DEVICE_TIMEOUT and exits; nothing faults or hangs. */
+FMLP_API fmlp_status fmlp_test_wait_timeout(int64_t timeout_us, fmlp_stream_t s);
+
+/* Static text for a status code. */
+FMLP_API const char* fmlp_status_string(fmlp_status st);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+FMLP_API const char* fmlp_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+FMLP_API int fmlp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FMLP_H_ */

@@ -1,0 +1,144 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/fmlp.h declares,
+validates arguments before touching any device, and its pure host functions are right."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import feed_forward_gemm_gb300 as fm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fmlp.h")
+
+A = 0x10000          # fake, 16-byte aligned "device" addresses; validation never dereferences
+GB = 1 << 30
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fm.build()
+    return fm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fmlp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("fmlp_linear_bias", "fmlp_mlp_gelu", "fmlp_geglu",
+                 "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
+                 "fmlp_status_string", "fmlp_last_error", "fmlp_device_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fmlp.h but not exported"
+    # and the Python binding forwards each under the same name
+    for name in declared_functions():
+        assert hasattr(fm, name), f"binding lacks {name}"
+
+
+def test_library_exports_nothing_else(lib):
+    out = os.popen(f"nm -D --defined-only {fm.library_path()}").read()
+    exported = sorted(set(re.findall(r"\sT\s+(\w+)", out)))
+    assert set(exported) == set(declared_functions()), exported
+
+
+def test_status_strings(lib):
+    assert fm.fmlp_status_string(0) == "FMLP_OK"
+    for st in range(1, 9):
+        assert fm.fmlp_status_string(st).startswith("FMLP_ERR_")
+    assert fm.fmlp_version() >= 100
+
+
+def test_workspace_sizes_and_counts(lib):
+    # the [8192, 3072] bf16 intermediate of the GPT-2-small-shaped block: ~50 MB
+    assert fm.fmlp_geglu_workspace_size(8192, 768, 3072) == 50_331_648
+    assert fm.fmlp_mlp_gelu_workspace_size(4096, 4096, 4096, 4096) in (0, 4096 * 4096 * 2)
+    assert fm.fmlp_geglu_workspace_size(0, 768, 3072) == 0
+
+
+def test_plans_are_pure_host(lib):
+    assert fm.fmlp_geglu_plan(0, 768, 3072) == fm.FMLP_PLAN_NONE
+    assert fm.fmlp_geglu_plan(8192, 768, 3072) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_linear_plan(1024, 32, 64) in (fm.FMLP_PLAN_TC, fm.FMLP_PLAN_GEMV)
+    assert fm.fmlp_mlp_gelu_plan(4096, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+
+
+def call_linear(x=A, W=A + GB, b=A + 2 * GB, y=A + 3 * GB, T=16, i=32, o=64):
+    return fm.fmlp_linear_bias(x, W, b, y, T, i, o, stream=0, raise_on_error=False)
+
+
+def test_linear_validation(lib):
+    assert call_linear(x=0) == fm.FMLP_ERR_NULL
+    assert call_linear(W=0) == fm.FMLP_ERR_NULL
+    assert call_linear(y=0) == fm.FMLP_ERR_NULL
+    assert call_linear(T=-1) == fm.FMLP_ERR_SHAPE
+    assert call_linear(i=0) == fm.FMLP_ERR_SHAPE
+    assert call_linear(i=12) == fm.FMLP_ERR_SHAPE          # not a multiple of 8
+    assert call_linear(o=2**31) == fm.FMLP_ERR_SHAPE
+    assert call_linear(x=A + 8) == fm.FMLP_ERR_ALIGN
+    assert call_linear(b=A + 2 * GB + 2) == fm.FMLP_ERR_ALIGN
+    assert call_linear(y=A + 16) == fm.FMLP_ERR_ALIAS       # y overlaps x
+    assert call_linear(y=A + GB) == fm.FMLP_ERR_ALIAS       # y overlaps W
+    assert "overlaps" in fm.fmlp_last_error()
+    # T == 0 is a no-op that succeeds without touching pointers or the device
+    assert call_linear(T=0, x=0, y=0) == fm.FMLP_OK
+
+
+def test_geglu_validation(lib):
+    def call(**kw):
+        a = dict(x=A, Wg=A + GB, Wu=A + 2 * GB, Wd=A + 3 * GB, y=A + 4 * GB, T=128, D=64,
+                 H=128, ws=A + 5 * GB, ws_bytes=128 * 128 * 2)
+        a.update(kw)
+        return fm.fmlp_geglu(a["x"], a["Wg"], a["Wu"], a["Wd"], a["y"], a["T"], a["D"], a["H"],
+                             a["ws"], a["ws_bytes"], stream=0, raise_on_error=False)
+    assert call(Wu=0) == fm.FMLP_ERR_NULL
+    assert call(H=100) == fm.FMLP_ERR_SHAPE
+    assert call(ws_bytes=100) == fm.FMLP_ERR_WORKSPACE
+    assert call(ws=A + 4 * GB) == fm.FMLP_ERR_ALIAS         # workspace on top of y
+    assert call(ws=A + 3 * GB) == fm.FMLP_ERR_ALIAS         # workspace on top of Wd
+    assert call(y=A + 2 * GB + 64) == fm.FMLP_ERR_ALIAS
+    assert call(Wd=A + 3 * GB + 4) == fm.FMLP_ERR_ALIGN
+    assert call(T=0) == fm.FMLP_OK
+
+
+def test_mlp_validation(lib):
+    def call(**kw):
+        a = dict(x=A, W1=A + GB, b1=A + 2 * GB, W2=A + 3 * GB, b2=A + 4 * GB, y=A + 5 * GB,
+                 T=4, D=64, H=64, Do=64, mode=fm.FMLP_GELU_ERF, ws=A + 6 * GB, ws_bytes=1 << 20)
+        a.update(kw)
+        return fm.fmlp_mlp_gelu(a["x"], a["W1"], a["b1"], a["W2"], a["b2"], a["y"], a["T"],
+                                a["D"], a["H"], a["Do"], a["mode"], a["ws"], a["ws_bytes"],
+                                stream=0, raise_on_error=False)
+    assert call(W2=0) == fm.FMLP_ERR_NULL
+    assert call(mode=7) == fm.FMLP_ERR_SHAPE
+    assert call(Do=6) == fm.FMLP_ERR_SHAPE
+    assert call(y=A + 4 * GB) == fm.FMLP_ERR_ALIAS          # y on top of b2
+    assert call(T=0) == fm.FMLP_OK
+
+
+def test_errors_raise_in_python(lib):
+    with pytest.raises(fm.FmlpError) as e:
+        fm.fmlp_linear_bias(0, A, None, A + GB, 8, 32, 64, stream=0)
+    assert e.value.status == fm.FMLP_ERR_NULL and "x is NULL" in str(e.value)
+
+
+def test_gelu_eval_and_timeout_validation(lib):
+    assert fm.fmlp_gelu_eval(A, A + GB, -1, stream=0, raise_on_error=False) == fm.FMLP_ERR_SHAPE
+    assert fm.fmlp_gelu_eval(A, A + GB, 4, mode=3, stream=0,
+                             raise_on_error=False) == fm.FMLP_ERR_SHAPE
+    assert fm.fmlp_gelu_eval(0, 0, 0, stream=0, raise_on_error=False) == fm.FMLP_OK
+    assert fm.fmlp_test_wait_timeout(0, stream=0, raise_on_error=False) == fm.FMLP_ERR_SHAPE
+
+
+def test_binding_refuses_noncontiguous(lib):
+    import torch
+    t = torch.zeros(4, 8)[:, ::2]
+    with pytest.raises(ValueError):
+        fm.fmlp_linear_bias(t, A, None, A + GB, 4, 8, 8, stream=0)

@@ -37,11 +37,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--steps", type=int, default=150)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-extras", action="store_true", help="headline only")
     p.add_argument("--cpu-sample-rows", type=int, default=0)
+    p.add_argument("--profile-kernel", default=None,
+                   choices=["gate_up", "down", "geglu", "mlp_up", "mlp", "linear"],
+                   help="profiling aid: launch one entry point --launches times on random "
+                        "inputs of --shape and exit (no timing, no JSON)")
+    p.add_argument("--shape", default="8192,8192,8192", help="T,D,H for --profile-kernel")
+    p.add_argument("--launches", type=int, default=3)
     return p.parse_args()
 
 
@@ -307,6 +313,23 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     def up(a):
         return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
 
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def cold_time(fn, iters):
+        """ms per call of fn() with L2 flushed (256 MB written) before every call; only the
+        call itself sits between the two events."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        fn()
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
     # GPT-2-small-shaped GeGLU FFN
     w = synth.WORKLOADS["geglu_8192x768x3072"]
     t = w.generate()
@@ -314,19 +337,11 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     y = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
     wsb = fm.fmlp_geglu_workspace_size(w.T, w.D, w.H)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def geglu4():
-        flush.zero_()   # evict L2 (256 MB > 129 MB) so weights come from HBM
-
-    fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream)
-    t_flush = events_time(geglu4, 10)
-    t_all = events_time(lambda: (geglu4(), fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws,
-                                                         wsb, stream)), 20)
-    ms = max(t_all - t_flush, 1e-6)
+    ms = cold_time(lambda: fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream), 30)
     out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
                    "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                   "l2": "flushed between iterations (256 MB write), flush time subtracted"}
+                   "plan": fm.fmlp_geglu_plan(w.T, w.D, w.H),
+                   "l2": "flushed before every call (median of 30)"}
     del x, Wg, Wu, Wd, y, ws
 
     # 4096-wide Linear -> GELU(erf) -> Linear with biases at 4096 tokens
@@ -340,12 +355,11 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     def mlp():
         fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, w.T, w.D, w.H, w.Dout,
                          fm.FMLP_GELU_ERF, ws, wsb, stream)
-    mlp()
-    t_all = events_time(lambda: (geglu4(), mlp()), 20)
-    ms = max(t_all - t_flush, 1e-6)
+    ms = cold_time(mlp, 30)
     out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
                    "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                   "l2": "flushed between iterations, flush time subtracted"}
+                   "plan": fm.fmlp_mlp_gelu_plan(w.T, w.D, w.H, w.Dout),
+                   "l2": "flushed before every call (median of 30)"}
     del d, y, ws
 
     # the same MLP at one token (decode): weights rotate through 5 copies (320 MB > 2x L2)
@@ -406,7 +420,7 @@ def cpu_baseline(t, w, rows_req: int):
 
     import oracle
     nthreads = oracle.threads()
-    rows_n = rows_req or max(2, min(64, nthreads))
+    rows_n = rows_req or 24 * nthreads   # about 10 s on 16 cores
     rows = np.arange(rows_n, dtype=np.int64)
     t0 = time.perf_counter()
     oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"], rows=rows, nthreads=nthreads)
@@ -457,8 +471,53 @@ def run_reference(args, dist: Dist):
     }
 
 
+def run_profile_case(args):
+    """Launch one entry point a few times on device-random inputs (for ncu captures)."""
+    import torch
+
+    import feed_forward_gemm_gb300 as fm
+    T, D, H = (int(v) for v in args.shape.split(","))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fm.load()
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+
+    def rnd(*shape, scale=1.0):
+        return (torch.randn(shape, generator=g, device=dev) * scale).to(torch.bfloat16)
+
+    x = rnd(T, D)
+    W1, W2, W3 = rnd(H, D, scale=D ** -0.5), rnd(H, D, scale=D ** -0.5), rnd(D, H, scale=H ** -0.5)
+    b1, b2 = rnd(H, scale=0.1), rnd(D, scale=0.1)
+    mid = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    k = args.profile_kernel
+    for _ in range(args.launches):
+        if k == "gate_up":
+            fm.fmlp_geglu_gate_up(x, W1, W2, mid, T, D, H)
+        elif k == "down":
+            fm.fmlp_linear_bias(mid, W3, None, y, T, H, D)
+        elif k == "geglu":
+            fm.fmlp_geglu(x, W1, W2, W3, y, T, D, H, mid, mid.numel() * 2)
+        elif k == "mlp_up":
+            fm.fmlp_linear_bias_gelu(x, W1, b1, mid, T, D, H, fm.FMLP_GELU_ERF)
+        elif k == "mlp":
+            fm.fmlp_mlp_gelu(x, W1, b1, W3, b2, y, T, D, H, D, fm.FMLP_GELU_ERF, mid,
+                             mid.numel() * 2)
+        elif k == "linear":
+            fm.fmlp_linear_bias(x, W1, b1, mid, T, D, H)
+    torch.cuda.synchronize()
+    st = fm.fmlp_device_status()
+    if st != fm.FMLP_OK:
+        raise SystemExit(f"device status {st}: {fm.fmlp_last_error()}")
+    print(f"profile case {k} {T}x{D}x{H}: {args.launches} launches ok")
+
+
 def main():
     args = parse()
+    if args.profile_kernel:
+        run_profile_case(args)
+        return
     dist = Dist(args.gpus)
     if args.impl == "reference":
         out = run_reference(args, dist)

@@ -22,7 +22,8 @@ __all__ = [
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
     "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
-    "fmlp_version",
+    "fmlp_version", "fmlp_set_tile_policy", "FMLP_TILES_AUTO", "FMLP_TILES_SINGLE",
+    "FMLP_TILES_PAIR",
     "FMLP_OK", "FMLP_ERR_NULL", "FMLP_ERR_SHAPE", "FMLP_ERR_ALIGN", "FMLP_ERR_ALIAS",
     "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
     "FMLP_GELU_TANH", "FMLP_GELU_ERF", "FMLP_PLAN_NONE", "FMLP_PLAN_TC",
@@ -33,6 +34,7 @@ FMLP_OK, FMLP_ERR_NULL, FMLP_ERR_SHAPE, FMLP_ERR_ALIGN, FMLP_ERR_ALIAS = 0, 1, 2
 FMLP_ERR_WORKSPACE, FMLP_ERR_CUDA, FMLP_ERR_DEVICE_TIMEOUT, FMLP_ERR_DEVICE = 5, 6, 7, 8
 FMLP_GELU_TANH, FMLP_GELU_ERF = 0, 1
 FMLP_PLAN_NONE, FMLP_PLAN_TC, FMLP_PLAN_FUSED_SMALL, FMLP_PLAN_GEMV = 0, 1, 2, 3
+FMLP_TILES_AUTO, FMLP_TILES_SINGLE, FMLP_TILES_PAIR = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +62,7 @@ _SIGNATURES = {
     "fmlp_status_string": (ctypes.c_char_p, [_INT]),
     "fmlp_last_error": (ctypes.c_char_p, []),
     "fmlp_version": (_INT, []),
+    "fmlp_set_tile_policy": (_INT, [_INT]),
 }
 
 
@@ -203,6 +206,11 @@ def fmlp_linear_plan(T, in_dim, out_dim) -> int:
 def fmlp_gelu_eval(x, out, n, mode=FMLP_GELU_TANH, stream=None, raise_on_error=True):
     st = load().fmlp_gelu_eval(_ptr(x), _ptr(out), n, int(mode), _stream(stream))
     return _check(st, "fmlp_gelu_eval", raise_on_error)
+
+
+def fmlp_set_tile_policy(policy: int, raise_on_error=True):
+    st = load().fmlp_set_tile_policy(int(policy))
+    return _check(st, "fmlp_set_tile_policy", raise_on_error)
 
 
 def fmlp_device_status(stream=None) -> int:

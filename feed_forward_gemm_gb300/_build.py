@@ -86,7 +86,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
-def kernel_fingerprint(names=("gemm_tc.cu", "ptx.cuh", "activation.cuh")) -> str:
+def kernel_fingerprint(names=("gemm_tc.cu", "gemm_tc2.cu", "gemm_epilogue.cuh", "ptx.cuh",
+                             "activation.cuh")) -> str:
     """Short hash of the kernel sources a profile was taken on."""
     h = hashlib.sha256()
     for n in names:

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -44,8 +45,11 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int major = 0, minor = 0;
+  int max_pairs = 0;   // co-resident CTA pairs of the pair GEMM (0: pair kernel unavailable)
   int* status = nullptr;
 };
+
+std::atomic<int> g_tile_policy{FMLP_TILES_AUTO};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -90,6 +94,10 @@ fmlp_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status)");
     d.status = static_cast<int*>(p);
+    if (gemm_tc2_max_pairs(&d.max_pairs) != cudaSuccess) {
+      d.max_pairs = 0;
+      (void)cudaGetLastError();
+    }
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -201,7 +209,7 @@ size_t mat_bytes(int64_t r, int64_t c) { return static_cast<size_t>(r) * static_
 // Persistent grid: each CTA takes tiles round-robin, so the critical path is
 // ceil(tiles / SMs) tiles of work proportional to bn. Narrow tiles cost extra shared-memory
 // bandwidth per FLOP; the efficiency factors reflect that.
-int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu) {
+int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu, double* cost_out) {
   const int cands[3] = {64, 128, 256};
   const double eff[3] = {0.60, 0.85, 1.0};
   int best = 0;
@@ -219,8 +227,13 @@ int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu) {
       best_cost = std::min(best_cost, cost);
     }
   }
+  *cost_out = best_cost;
   return best;
 }
+
+// The CTA-pair kernel computes 256x256 tiles with two SMs; per SM that is the work of one
+// 128x256 single-SM tile with a third less operand traffic, hence its efficiency edge.
+constexpr double kPairEff = 1.15;
 
 fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
                         const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
@@ -228,8 +241,21 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   GemmLaunch L;
   memset(&L, 0, sizeof L);
   const bool geglu = epi == EPI_GEGLU;
-  L.bn = pick_bn(M, N_out, d.sms, geglu);
-  const uint32_t b_rows = geglu ? L.bn / 2 : L.bn;
+  double cost1 = 0;
+  L.bn = pick_bn(M, N_out, d.sms, geglu, &cost1);
+  const int policy = g_tile_policy.load(std::memory_order_relaxed);
+  bool pair = false;
+  int pairs = 0;
+  if (d.max_pairs >= 1 && M > 128 && policy != FMLP_TILES_SINGLE) {
+    const int bn_out2 = geglu ? 128 : 256;
+    const int64_t tiles2 = ((M + 255) / 256) * ((N_out + bn_out2 - 1) / bn_out2);
+    pairs = static_cast<int>(std::min<int64_t>(tiles2, d.max_pairs));
+    const int64_t waves2 = (tiles2 + pairs - 1) / pairs;
+    const double cost2 = static_cast<double>(waves2) * 256 / kPairEff;
+    pair = policy == FMLP_TILES_PAIR || cost2 < cost1;
+  }
+  if (pair) L.bn = 256;
+  const uint32_t b_rows = pair ? 128u : (geglu ? L.bn / 2 : L.bn);
   FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A"));
   FMLP_TRY(make_map(&L.tmB0, B0, N_out, K, b_rows, "B"));
   if (geglu) {
@@ -244,15 +270,100 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   L.K = static_cast<int>(K);
   L.gelu_mode = gelu_mode;
   L.epi = epi;
-  const int bn_out = geglu ? L.bn / 2 : L.bn;
-  const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
-  L.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
   L.pdl = pdl;
   L.stream = s;
   L.status = d.status;
   L.timeout_ns = kWaitTimeoutNs;
-  cudaError_t e = gemm_tc_launch(L);
-  if (e != cudaSuccess) return cuda_fail(e, "gemm_tc launch");
+  cudaError_t e;
+  if (pair) {
+    L.grid = 2 * pairs;
+    e = gemm_tc2_launch(L);
+  } else {
+    const int bn_out = geglu ? L.bn / 2 : L.bn;
+    const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
+    L.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
+    e = gemm_tc_launch(L);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, pair ? "gemm_tc2 launch" : "gemm_tc launch");
+  return FMLP_OK;
+}
+
+// ------------------------------------------------------------------------- plans
+
+// The device SM count for host-only plan queries when no device state exists yet; the GEMV
+// smem bound depends on the grid only through rows per CTA, and GB300 has 152 SMs.
+constexpr int kPlanSms = 152;
+
+bool gemv_ok(int64_t T, int64_t K, int64_t N, int nmat, int sms) {
+  if (T < 1 || T > kGemvMaxT || K % 256 != 0) return false;
+  const int grid = static_cast<int>(std::min<int64_t>(N, sms));
+  return gemv_smem_bytes(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), nmat,
+                         grid) <= kGemvMaxSmem;
+}
+
+int plan_linear(int64_t T, int64_t in, int64_t out, int sms) {
+  if (T <= 0) return FMLP_PLAN_NONE;
+  return gemv_ok(T, in, out, 1, sms) ? FMLP_PLAN_GEMV : FMLP_PLAN_TC;
+}
+
+int plan_mlp(int64_t T, int64_t D, int64_t H, int64_t Dout, int sms) {
+  if (T <= 0) return FMLP_PLAN_NONE;
+  if (gemv_ok(T, D, H, 1, sms) && gemv_ok(T, H, Dout, 1, sms)) return FMLP_PLAN_GEMV;
+  return FMLP_PLAN_TC;
+}
+
+// The fused single-kernel plan depends on the shape alone (never on the SM count), so the
+// workspace query and the call always agree on whether m needs a workspace.
+int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
+  if (T <= 0) return FMLP_PLAN_NONE;
+  const bool gemv_shape = T <= kGemvMaxT && D % 256 == 0 && H % 256 == 0;
+  if (gemv_shape) {
+    if (gemv_ok(T, D, H, 2, sms) && gemv_ok(T, H, D, 1, sms)) return FMLP_PLAN_GEMV;
+    return FMLP_PLAN_TC;
+  }
+  if (D <= kSmallMaxD && D % 16 == 0 && H <= kSmallMaxH) return FMLP_PLAN_FUSED_SMALL;
+  return FMLP_PLAN_TC;
+}
+
+fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void* W0,
+                        const void* W1, const void* bias, void* y, int64_t T, int64_t K,
+                        int64_t N, int gelu_mode, cudaStream_t s) {
+  GemvLaunch L;
+  L.x = x;
+  L.W0 = W0;
+  L.W1 = W1;
+  L.bias = bias;
+  L.y = y;
+  L.T = static_cast<int>(T);
+  L.K = static_cast<int>(K);
+  L.N = static_cast<int>(N);
+  L.epi = epi;
+  L.gelu_mode = gelu_mode;
+  L.grid = static_cast<int>(std::min<int64_t>(N, d.sms));
+  L.stream = s;
+  cudaError_t e = gemv_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+  return FMLP_OK;
+}
+
+fmlp_status launch_small(const DeviceState& d, const void* x, const void* Wg, const void* Wu,
+                         const void* Wd, void* y, int64_t T, int64_t D, int64_t H,
+                         cudaStream_t s) {
+  SmallLaunch L;
+  memset(&L, 0, sizeof L);
+  FMLP_TRY(make_map(&L.tmX, x, T, D, 128, "x"));
+  FMLP_TRY(make_map(&L.tmWg, Wg, H, D, 64, "Wg"));
+  FMLP_TRY(make_map(&L.tmWu, Wu, H, D, 64, "Wu"));
+  FMLP_TRY(make_map(&L.tmWd, Wd, D, H, static_cast<uint32_t>(D), "Wd"));
+  FMLP_TRY(make_map(&L.tmY, y, T, D, 32, "y"));
+  L.T = static_cast<int>(T);
+  L.D = static_cast<int>(D);
+  L.H = static_cast<int>(H);
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
+  L.stream = s;
+  cudaError_t e = ffn_small_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "fused small launch");
   return FMLP_OK;
 }
 
@@ -283,35 +394,23 @@ const char* fmlp_status_string(fmlp_status st) {
 const char* fmlp_last_error(void) { return t_last_error.c_str(); }
 
 size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
-  (void)D;
-  if (T <= 0 || H <= 0) return 0;
-  return mat_bytes(T, H);
+  const int p = plan_geglu(T, D, H, kPlanSms);
+  return (p == FMLP_PLAN_TC || p == FMLP_PLAN_GEMV) ? mat_bytes(T, H) : 0;
 }
 
 size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout) {
-  (void)D;
-  (void)Dout;
-  if (T <= 0 || H <= 0) return 0;
+  if (plan_mlp(T, D, H, Dout, kPlanSms) == FMLP_PLAN_NONE) return 0;
   return mat_bytes(T, H);
 }
 
-int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) {
-  (void)D;
-  (void)H;
-  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
-}
+int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) { return plan_geglu(T, D, H, kPlanSms); }
 
 int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout) {
-  (void)D;
-  (void)H;
-  (void)Dout;
-  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
+  return plan_mlp(T, D, H, Dout, kPlanSms);
 }
 
 int fmlp_linear_plan(int64_t T, int64_t in, int64_t out) {
-  (void)in;
-  (void)out;
-  return T <= 0 ? FMLP_PLAN_NONE : FMLP_PLAN_TC;
+  return plan_linear(T, in, out, kPlanSms);
 }
 
 static fmlp_status linear_common(const void* x, const void* W, const void* b, void* y,
@@ -337,8 +436,10 @@ static fmlp_status linear_common(const void* x, const void* W, const void* b, vo
   FMLP_TRY(check_alias(ry, ins, 3));
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
-  return launch_gemm(*d, epi, x, W, nullptr, b, y, T, out, in, mode, false,
-                     reinterpret_cast<cudaStream_t>(s));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  if (plan_linear(T, in, out, d->sms) == FMLP_PLAN_GEMV)
+    return launch_gemv(*d, epi, x, W, nullptr, b, y, T, in, out, mode, st);
+  return launch_gemm(*d, epi, x, W, nullptr, b, y, T, out, in, mode, false, st);
 }
 
 fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y, int64_t T,
@@ -371,8 +472,10 @@ fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, vo
   FMLP_TRY(check_alias(rm, ins, 3));
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
-  return launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false,
-                     reinterpret_cast<cudaStream_t>(s));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  if (gemv_ok(T, D, H, 2, d->sms))
+    return launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st);
+  return launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
 }
 
 fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
@@ -405,13 +508,22 @@ fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int plan = plan_geglu(T, D, H, d->sms);
+  if (plan == FMLP_PLAN_FUSED_SMALL) return launch_small(*d, x, Wg, Wu, Wd, y, T, D, H, st);
   void* m = ws;
   if (!m) {
     cudaError_t e = cudaMallocAsync(&m, need, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
   }
-  fmlp_status r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
-  if (r == FMLP_OK) r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st);
+  fmlp_status r;
+  if (plan == FMLP_PLAN_GEMV) {
+    r = launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st);
+    if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st);
+  } else {
+    r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
+    if (r == FMLP_OK)
+      r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st);
+  }
   if (!ws) {
     cudaError_t e = cudaFreeAsync(m, st);
     if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
@@ -459,14 +571,30 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
     cudaError_t e = cudaMallocAsync(&h, need, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
   }
-  fmlp_status r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D,
-                              static_cast<int>(mode), false, st);
-  if (r == FMLP_OK) r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st);
+  fmlp_status r;
+  if (plan_mlp(T, D, H, Dout, d->sms) == FMLP_PLAN_GEMV) {
+    r = launch_gemv(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, D, H, static_cast<int>(mode), st);
+    if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st);
+  } else {
+    r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D, static_cast<int>(mode),
+                    false, st);
+    if (r == FMLP_OK)
+      r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st);
+  }
   if (!ws) {
     cudaError_t e = cudaFreeAsync(h, st);
     if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
   }
   return r;
+}
+
+fmlp_status fmlp_set_tile_policy(int policy) {
+  if (policy != FMLP_TILES_AUTO && policy != FMLP_TILES_SINGLE && policy != FMLP_TILES_PAIR) {
+    set_error("tile policy %d unknown", policy);
+    return FMLP_ERR_SHAPE;
+  }
+  g_tile_policy.store(policy, std::memory_order_relaxed);
+  return FMLP_OK;
 }
 
 fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,

@@ -28,6 +28,7 @@
 // both share the A tile and the same instruction.
 // All waits are bounded; on expiry the kernel records a status code and unwinds.
 #include "activation.cuh"
+#include "gemm_epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,7 +38,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;                 // 64 bf16 = 128 bytes = one swizzle row
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr int kStgBytes = 32 * 128;     // one staging tile: 32 rows x 64 bf16
 constexpr int kRasterGroup = 16;        // M tiles per raster group (L2 reuse of weights)
 
 template <int BN, int EPI>
@@ -226,73 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
       const int row0 = tm * kBM + wq * 32;
-#pragma unroll 1
-      for (int ch = 0; ch < C::BN_OUT / 64; ++ch) {
-        const int n_chunk = tn * C::BN_OUT + ch * 64;
-        uint8_t* sbuf = stg + sb * kStgBytes;
-        // the TMA store that last read this staging buffer must be done reading it
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = ch * 64 + h * 32;
-          uint32_t acc[32];
-          tmem_ld_32x32b_x32(t_row + c, acc);
-          float v[32];
-          if (EPI == EPI_GEGLU) {
-            uint32_t up[32];
-            tmem_ld_32x32b_x32(t_row + BN / 2 + c, up);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              v[i] = gelu_tanh_f(__uint_as_float(acc[i])) * __uint_as_float(up[i]);
-          } else {
-            tmem_ld_wait();
-            float bv[32];
-            const int nb = n_chunk + h * 32;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w = make_uint4(0u, 0u, 0u, 0u);
-              if (bias != nullptr && nb + q * 8 < N_out)
-                w = __ldg(reinterpret_cast<const uint4*>(bias + nb + q * 8));
-              bv[q * 8 + 0] = bf16_lo(w.x);
-              bv[q * 8 + 1] = bf16_hi(w.x);
-              bv[q * 8 + 2] = bf16_lo(w.y);
-              bv[q * 8 + 3] = bf16_hi(w.y);
-              bv[q * 8 + 4] = bf16_lo(w.z);
-              bv[q * 8 + 5] = bf16_hi(w.z);
-              bv[q * 8 + 6] = bf16_lo(w.w);
-              bv[q * 8 + 7] = bf16_hi(w.w);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float z = __uint_as_float(acc[i]) + bv[i];
-              v[i] = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
-            }
-          }
-          // 32 values = 4 x 16 bytes; 16-byte chunk j of this row goes to slot j ^ (row & 7)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j = h * 4 + q;
-            const uint32_t addr = smem_u32(sbuf) + static_cast<uint32_t>(lane * 128) +
-                                  static_cast<uint32_t>(((j ^ (lane & 7)) << 4));
-            const uint32_t p0 = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-            const uint32_t p1 = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-            const uint32_t p2 = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-            const uint32_t p3 = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p0),
-                         "r"(p1), "r"(p2), "r"(p3)
-                         : "memory");
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (row0 < M && n_chunk < N_out) tma_store_2d(&tmY, sbuf, n_chunk, row0);
-          bulk_commit_group();
-        }
-        sb ^= 1;
-      }
+      epilogue_rows<BN, C::BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * C::BN_OUT, M, N_out,
+                                        &tmY, bias, gelu_mode);
       // this warp is done reading the accumulator buffer
       tc_fence_before();
       mbar_arrive(&tempty[buf]);

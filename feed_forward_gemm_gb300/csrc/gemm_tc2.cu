@@ -1,0 +1,288 @@
+// CTA-pair (cta_group::2) variant of the persistent tcgen05 GEMM, for large problems.
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 accumulator tile with one MMA stream:
+// the even CTA issues tcgen05.mma.cta_group::2 with M = 256, N = 256, K = 16, whose A operand
+// is 128 rows from each CTA's shared memory and whose B operand is 128 rows from each CTA's
+// shared memory; each CTA's TMEM receives its own 128 rows of D (all 256 columns). Per SM
+// and per 64-wide K step that is 16 KB of A plus 16 KB of B instead of 16 KB plus 32 KB for a
+// single-SM 128 x 256 tile: a third less shared-memory and L2 traffic for the same MMA work.
+//
+// For GeGLU the even CTA loads the gate weight rows and the odd CTA the matching up weight
+// rows, so D columns [0, 128) are g and [128, 256) are u for all 256 tokens, and each CTA's
+// epilogue forms m = bf16(gelu_tanh(g) * u) for its 128 tokens.
+//
+// Synchronisation:
+//   full[s]    (even CTA) one arrive.expect_tx for both CTAs' bytes; both CTAs' TMA loads
+//              complete on it (.cta_group::2 lets a load signal the peer's barrier).
+//   empty[s]   (both CTAs) the even CTA's tcgen05.commit multicasts to both.
+//   tfull[b]   (both CTAs) accumulator b ready, multicast commit.
+//   tempty[b]  (even CTA) 256 arrivals: every epilogue thread of both CTAs.
+// Cluster barriers bracket the kernel so neither CTA leaves while the other may still touch
+// its shared memory or TMEM. Every mbarrier wait is bounded.
+#include "activation.cuh"
+#include "gemm_epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmlp {
+
+namespace {
+
+constexpr int kPairBN = 256;             // MMA N (both CTAs together)
+constexpr int kPairBK = 64;
+constexpr int kPairThreads = 192;
+constexpr int kPairEpiWarps = 4;
+constexpr int kPairGroup = 8;            // pair M tiles (256 rows) per raster group
+constexpr int kPairA = 128 * 128;        // 128 rows x 64 bf16
+constexpr int kPairB = 128 * 128;        // this CTA's 128 B rows x 64 bf16
+constexpr int kPairStage = kPairA + kPairB;
+constexpr int kPairStages = 6;
+constexpr int kPairBar = (2 * kPairStages + 5) * 8 + 16;
+constexpr int kPairSmem = 1024 + kPairStages * kPairStage + kPairEpiWarps * 2 * kStgBytes + kPairBar;
+static_assert(kPairSmem <= 232448, "shared memory");
+
+__device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, int& tm, int& tn) {
+  const int per_group = kPairGroup * num_n;
+  const int g = t / per_group;
+  const int first_m = g * kPairGroup;
+  const int gm = min(num_m - first_m, kPairGroup);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+}  // namespace
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ CUtensorMap tmY,
+                    const __nv_bfloat16* __restrict__ bias, int M, int N_out, int K,
+                    int gelu_mode, int* status, uint64_t timeout_ns) {
+  constexpr int BN_OUT = EPI == EPI_GEGLU ? kPairBN / 2 : kPairBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  uint8_t* stg_all = smem + kPairStages * kPairStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_all + kPairEpiWarps * 2 * kStgBytes);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: issues the MMAs, 1: its peer
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmY);
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kPairEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // barriers of both CTAs initialised before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  pdl_wait_primary();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  const int num_m = (M + 2 * 128 - 1) / (2 * 128);
+  const int num_n = (N_out + BN_OUT - 1) / BN_OUT;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (K + kPairBK - 1) / kPairBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // even CTA's full[0]
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_phase_mask = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        int tm, tn;
+        pair_tile_coords(t, num_m, num_n, tm, tn);
+        const int a_row = tm * 256 + static_cast<int>(rank) * 128;
+        const CUtensorMap* bmap = &tmB0;
+        int b_row;
+        if (EPI == EPI_GEGLU) {
+          bmap = rank == 0 ? &tmB0 : &tmB1;   // gate rows on the even CTA, up rows on the odd
+          b_row = tn * 128;
+        } else {
+          b_row = tn * 256 + static_cast<int>(rank) * 128;
+        }
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, status, SITE_PRODUCER_EMPTY, timeout_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = stages + stage * kPairStage;
+          uint8_t* sB = sA + kPairA;
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
+          const uint32_t fb = full0 + static_cast<uint32_t>(stage * 8);
+          tma_load_2d_pair(sA, &tmA, fb, kb * kPairBK, a_row);
+          tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
+          issued_mask |= 1u << stage;
+          last_phase_mask = (last_phase_mask & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // loads land on the even CTA's barriers; it waits for all of them before exiting
+      if (rank == 0)
+        for (int s = 0; s < kPairStages; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait(&full[s], (last_phase_mask >> s) & 1u, status, SITE_DRAIN, timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(256, kPairBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = pair; t < num_tiles && ok; t += npairs, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], use ^ 1u, status, SITE_MMA_TMEM_EMPTY, timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kPairBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, status, SITE_MMA_FULL, timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + stage * kPairStage);
+          const uint64_t a_desc = sdesc_kmajor_sw128(a_addr);
+          const uint64_t b_desc = sdesc_kmajor_sw128(a_addr + kPairA);
+#pragma unroll
+          for (int kk = 0; kk < kPairBK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+                             (kb | kk) != 0 ? 1u : 0u);
+          tc_commit_pair_mc(&empty[stage], 0x3);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&tfull[buf], 0x3);
+      }
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, status, SITE_DRAIN, timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int wq = warp & 3;
+    uint8_t* stg = stg_all + (warp - 2) * 2 * kStgBytes;
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+    int sb = 0;
+    int it = 0;
+    for (int t = pair; t < num_tiles; t += npairs, ++it) {
+      int tm, tn;
+      pair_tile_coords(t, num_m, num_n, tm, tn);
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      const bool ok = mbar_wait(&tfull[buf], use, status, SITE_EPI_TMEM_FULL, timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
+                             static_cast<uint32_t>(buf * kPairBN);
+      const int row0 = tm * 256 + static_cast<int>(rank) * 128 + wq * 32;
+      epilogue_rows<kPairBN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
+                                          &tmY, bias, gelu_mode);
+      tc_fence_before();
+      mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf * 8));
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer's MMAs, loads and arrivals are finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+int gemm_tc2_smem_bytes() { return kPairSmem; }
+
+template <int EPI>
+static cudaError_t launch_pair(const GemmLaunch& L) {
+  auto kern = gemm_tc2_kernel<EPI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = L.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB0, L.tmB1, L.tmY,
+                            static_cast<const __nv_bfloat16*>(L.bias), L.M, L.N_out, L.K,
+                            L.gelu_mode, L.status, L.timeout_ns);
+}
+
+cudaError_t gemm_tc2_launch(const GemmLaunch& L) {
+  if (L.grid < 2 || (L.grid & 1)) return cudaErrorInvalidValue;
+  switch (L.epi) {
+    case EPI_BIAS: return launch_pair<EPI_BIAS>(L);
+    case EPI_BIAS_GELU: return launch_pair<EPI_BIAS_GELU>(L);
+    case EPI_GEGLU: return launch_pair<EPI_GEGLU>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Largest number of co-resident CTA pairs (queried once per device by the host).
+cudaError_t gemm_tc2_max_pairs(int* pairs) {
+  auto kern = gemm_tc2_kernel<EPI_BIAS>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  *pairs = n;
+  return cudaSuccess;
+}
+
+}  // namespace fmlp

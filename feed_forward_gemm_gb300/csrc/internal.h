@@ -34,8 +34,48 @@ struct GemmLaunch {
 };
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
+// CTA-pair (cta_group::2) kernel: 256 x 256 tiles over clusters of two CTAs; bn is 256;
+// grid = 2 x pairs.
+cudaError_t gemm_tc2_launch(const GemmLaunch& L);
+int gemm_tc2_smem_bytes();
+cudaError_t gemm_tc2_max_pairs(int* pairs);
 // Dynamic shared memory a GEMM configuration needs (0 if the configuration does not exist).
 int gemm_tc_smem_bytes(int epi, int bn);
+
+// Weight-streaming GEMV for T <= kGemvMaxT tokens (decode).
+constexpr int kGemvMaxT = 4;
+constexpr size_t kGemvMaxSmem = 100 * 1024;  // two CTAs per SM for launch overlap
+struct GemvLaunch {
+  const void* x;      // [T, K]
+  const void* W0;     // [N, K]  (Wg for GeGLU)
+  const void* W1;     // [N, K]  Wu for GeGLU, else unused
+  const void* bias;   // [N] or nullptr
+  void* y;            // [T, N]
+  int T, K, N;
+  int epi;
+  int gelu_mode;
+  int grid;
+  cudaStream_t stream;
+};
+size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);
+cudaError_t gemv_launch(const GemvLaunch& L);
+
+// Whole GeGLU block in one kernel for small D (fused plan).
+constexpr int kSmallMaxD = 256;
+constexpr int kSmallMaxH = 2048;
+struct SmallLaunch {
+  CUtensorMap tmX;    // x  [T, D], box {64, 128}
+  CUtensorMap tmWg;   // Wg [H, D], box {64, 64}
+  CUtensorMap tmWu;   // Wu [H, D], box {64, 64}
+  CUtensorMap tmWd;   // Wd [D, H], box {64, D}
+  CUtensorMap tmY;    // y  [T, D], box {64, 32}
+  int T, D, H;
+  int* status;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+int ffn_small_smem_bytes(int D);
+cudaError_t ffn_small_launch(const SmallLaunch& L);
 
 // Device GELU check kernel.
 cudaError_t gelu_eval_launch(const float* in, float* out, int64_t n, int mode,

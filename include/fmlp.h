@@ -133,6 +133,13 @@ FMLP_API int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H);
 FMLP_API int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout);
 FMLP_API int fmlp_linear_plan(int64_t T, int64_t in, int64_t out);
 
+/* Tile-kernel policy for the tensor-core plans, process-wide (default FMLP_TILES_AUTO):
+ * AUTO picks per call from the shape; SINGLE forces one-SM 128-row tiles; PAIR forces two-SM
+ * (CTA pair, 256-row) tiles wherever the shape has more than 128 rows. Results are identical
+ * up to fp32 summation order. Returns FMLP_ERR_SHAPE for an unknown value. */
+typedef enum { FMLP_TILES_AUTO = 0, FMLP_TILES_SINGLE = 1, FMLP_TILES_PAIR = 2 } fmlp_tile_policy;
+FMLP_API fmlp_status fmlp_set_tile_policy(int policy);
+
 /* Device activation check: out[i] = GELU(in[i]) in fp32 with the exact device code the
  * epilogues use. in/out: n floats in device memory. One kernel. */
 FMLP_API fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,

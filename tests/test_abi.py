@@ -93,7 +93,7 @@ def test_linear_validation(lib):
 
 def test_geglu_validation(lib):
     def call(**kw):
-        a = dict(x=A, Wg=A + GB, Wu=A + 2 * GB, Wd=A + 3 * GB, y=A + 4 * GB, T=128, D=64,
+        a = dict(x=A, Wg=A + GB, Wu=A + 2 * GB, Wd=A + 3 * GB, y=A + 4 * GB, T=128, D=512,
                  H=128, ws=A + 5 * GB, ws_bytes=128 * 128 * 2)
         a.update(kw)
         return fm.fmlp_geglu(a["x"], a["Wg"], a["Wu"], a["Wd"], a["y"], a["T"], a["D"], a["H"],
@@ -142,3 +142,9 @@ def test_binding_refuses_noncontiguous(lib):
     t = torch.zeros(4, 8)[:, ::2]
     with pytest.raises(ValueError):
         fm.fmlp_linear_bias(t, A, None, A + GB, 4, 8, 8, stream=0)
+
+
+def test_tile_policy_validation(lib):
+    assert fm.fmlp_set_tile_policy(7, raise_on_error=False) == fm.FMLP_ERR_SHAPE
+    for p in (fm.FMLP_TILES_SINGLE, fm.FMLP_TILES_PAIR, fm.FMLP_TILES_AUTO):
+        assert fm.fmlp_set_tile_policy(p) == fm.FMLP_OK

@@ -1,0 +1,192 @@
+"""The fused single-kernel plan (small D) and the GEMV plan (a few tokens) against the oracle,
+and the number of kernels each plan launches (counted in a captured CUDA graph)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import feed_forward_gemm_gb300 as fm
+import oracle
+import synth
+from gpu_util import DEV, empty_bf16, guarded_bf16, to_dev, to_host, workspace
+from helpers import assert_parity, rne_bf16_array
+
+pytestmark = pytest.mark.gpu
+rng = np.random.default_rng(777)
+
+
+def ubits(shape, bound):
+    return rne_bf16_array(rng.uniform(-bound, bound, shape))
+
+
+def rbits(shape):
+    return rne_bf16_array(rng.standard_normal(shape))
+
+
+def geglu_inputs(T, D, H):
+    return (rbits((T, D)), ubits((H, D), 1 / math.sqrt(D)), ubits((H, D), 1 / math.sqrt(D)),
+            ubits((D, H), 1 / math.sqrt(H)))
+
+
+def run_geglu(x, Wg, Wu, Wd):
+    T, D = x.shape
+    H = Wg.shape[0]
+    _, y, check = guarded_bf16(T, D)
+    ws = workspace(fm.fmlp_geglu_workspace_size(T, D, H))
+    fm.fmlp_geglu(to_dev(x), to_dev(Wg), to_dev(Wu), to_dev(Wd), y, T, D, H, ws, ws.numel())
+    torch.cuda.synchronize()
+    check()
+    return to_host(y)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fm.load()
+    yield
+    assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
+
+
+# ------------------------------------------------------------------------ fused small plan
+
+@pytest.mark.parametrize("T,D,H", [(1, 32, 64), (100, 32, 64), (129, 16, 8), (1024, 32, 64),
+                                   (300, 64, 200), (257, 96, 520), (128, 128, 1000),
+                                   (513, 256, 2048), (64, 208, 72)])
+def test_fused_small_geglu_vs_oracle(T, D, H):
+    assert fm.fmlp_geglu_plan(T, D, H) == fm.FMLP_PLAN_FUSED_SMALL
+    assert fm.fmlp_geglu_workspace_size(T, D, H) == 0
+    x, Wg, Wu, Wd = geglu_inputs(T, D, H)
+    assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"fused {T}x{D}x{H}")
+
+
+def test_fused_small_special_cases():
+    T, D = 200, 64
+    x = rbits((T, D))
+    W = ubits((D, D), .2)
+    zero = np.zeros((D, D), np.uint16)
+    assert np.array_equal(run_geglu(x, zero, W, W), oracle.geglu(x, zero, W, W))
+    assert np.array_equal(run_geglu(x, W, zero, W), oracle.geglu(x, W, zero, W))
+    eye, two = rne_bf16_array(np.eye(D)), rne_bf16_array(2 * np.eye(D))
+    got, ref = run_geglu(x, eye, two, eye), oracle.geglu(x, eye, two, eye)
+    assert np.abs(got.astype(np.int32) - ref.astype(np.int32)).max() <= 1
+
+
+def test_fused_small_workload_and_determinism():
+    w = synth.WORKLOADS["geglu_1024x32x64"]
+    t = w.generate()
+    a = run_geglu(t["x"], t["Wg"], t["Wu"], t["Wd"])
+    b = run_geglu(t["x"], t["Wg"], t["Wu"], t["Wd"])
+    assert np.array_equal(a, b)
+    assert_parity(a, oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"]), "geglu 1024x32x64")
+
+
+# ------------------------------------------------------------------------ GEMV plan
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("K,N", [(256, 64), (512, 1000), (4096, 4096), (3072, 768)])
+def test_gemv_linear_vs_oracle(T, K, N):
+    assert fm.fmlp_linear_plan(T, K, N) == fm.FMLP_PLAN_GEMV
+    x, W, b = rbits((T, K)), ubits((N, K), 1 / math.sqrt(K)), ubits((N,), 1 / math.sqrt(K))
+    _, y, check = guarded_bf16(T, N)
+    fm.fmlp_linear_bias(to_dev(x), to_dev(W), to_dev(b), y, T, K, N)
+    torch.cuda.synchronize()
+    check()
+    assert_parity(to_host(y), oracle.linear(x, W, b), f"gemv {T}x{K}->{N}")
+
+
+@pytest.mark.parametrize("T,D,H", [(1, 256, 512), (2, 768, 3072), (4, 512, 1280)])
+def test_gemv_geglu_vs_oracle(T, D, H):
+    assert fm.fmlp_geglu_plan(T, D, H) == fm.FMLP_PLAN_GEMV
+    x, Wg, Wu, Wd = geglu_inputs(T, D, H)
+    assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"gemv geglu {T}x{D}x{H}")
+    # the gate/up stage on its own
+    m = empty_bf16(T, H)
+    fm.fmlp_geglu_gate_up(to_dev(x), to_dev(Wg), to_dev(Wu), m, T, D, H)
+    torch.cuda.synchronize()
+    _, ref_m = oracle.geglu(x, Wg, Wu, Wd, want_m=True)
+    assert_parity(to_host(m), ref_m, "gemv gate/up")
+
+
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH])
+def test_decode_mlp_4096_vs_oracle(mode):
+    w = synth.WORKLOADS["mlp_4096_t1"]
+    assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == fm.FMLP_PLAN_GEMV
+    t = w.generate()
+    d = {k: to_dev(v) for k, v in t.items()}
+    _, y, check = guarded_bf16(1, w.Dout)
+    ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, w.D, w.H, w.Dout))
+    fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, 1, w.D, w.H, w.Dout, mode,
+                     ws, ws.numel())
+    torch.cuda.synchronize()
+    check()
+    ref = oracle.mlp_gelu(t["x"], t["W1"], t["b1"], t["W2"], t["b2"],
+                          gelu_mode=oracle.GELU_ERF if mode == fm.FMLP_GELU_ERF else oracle.GELU_TANH)
+    assert_parity(to_host(y), ref, "decode mlp 4096")
+
+
+def test_gemv_deterministic_across_calls():
+    x, W, b = rbits((3, 4096)), ubits((4096, 4096), 1 / 64), ubits((4096,), 1 / 64)
+    outs = []
+    for _ in range(3):
+        y = empty_bf16(3, 4096)
+        fm.fmlp_linear_bias(to_dev(x), to_dev(W), to_dev(b), y, 3, 4096, 4096)
+        torch.cuda.synchronize()
+        outs.append(to_host(y))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# ------------------------------------------------------------------------ kernel counts
+
+def count_kernels_in_graph(fn):
+    from cuda.bindings import runtime as rt
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn(s)
+    torch.cuda.synchronize()
+    err, = rt.cudaStreamBeginCapture(s.cuda_stream, rt.cudaStreamCaptureMode.cudaStreamCaptureModeThreadLocal)[:1]
+    assert err == rt.cudaError_t.cudaSuccess
+    fn(s)
+    err, graph = rt.cudaStreamEndCapture(s.cuda_stream)
+    assert err == rt.cudaError_t.cudaSuccess
+    err, _, n = rt.cudaGraphGetNodes(graph, 0)
+    assert err == rt.cudaError_t.cudaSuccess
+    err, nodes, n = rt.cudaGraphGetNodes(graph, n)
+    kinds = []
+    for node in nodes[:n]:
+        err, ty = rt.cudaGraphNodeGetType(node)
+        kinds.append(ty)
+    rt.cudaGraphDestroy(graph)
+    return sum(1 for k in kinds if k == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel), len(kinds)
+
+
+@pytest.mark.parametrize("T,D,H,plan,kernels", [
+    (1024, 32, 64, fm.FMLP_PLAN_FUSED_SMALL, 1),
+    (1, 768, 3072, fm.FMLP_PLAN_GEMV, 2),
+    (512, 768, 3072, fm.FMLP_PLAN_TC, 2),
+])
+def test_geglu_kernel_count(T, D, H, plan, kernels):
+    pytest.importorskip("cuda.bindings")
+    assert fm.fmlp_geglu_plan(T, D, H) == plan
+    x, Wg, Wu, Wd = (to_dev(a) for a in geglu_inputs(T, D, H))
+    y = empty_bf16(T, D)
+    ws = workspace(fm.fmlp_geglu_workspace_size(T, D, H))
+    nk, nall = count_kernels_in_graph(
+        lambda s: fm.fmlp_geglu(x, Wg, Wu, Wd, y, T, D, H, ws, ws.numel(), stream=s))
+    assert nk == kernels and nall == kernels
+
+
+def test_linear_and_mlp_kernel_counts():
+    pytest.importorskip("cuda.bindings")
+    T, K, N = 1024, 32, 64
+    x, W, b = to_dev(rbits((T, K))), to_dev(ubits((N, K), .1)), to_dev(ubits((N,), .1))
+    y = empty_bf16(T, N)
+    nk, _ = count_kernels_in_graph(lambda s: fm.fmlp_linear_bias(x, W, b, y, T, K, N, stream=s))
+    assert nk == 1     # the bias add is the GEMM's epilogue: one kernel
+    x1 = to_dev(rbits((1, 4096)))
+    W1, W2 = to_dev(ubits((4096, 4096), 1 / 64)), to_dev(ubits((4096, 4096), 1 / 64))
+    b1, b2 = to_dev(ubits((4096,), 1 / 64)), to_dev(ubits((4096,), 1 / 64))
+    y1 = empty_bf16(1, 4096)
+    ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, 4096, 4096, 4096))
+    nk, _ = count_kernels_in_graph(lambda s: fm.fmlp_mlp_gelu(
+        x1, W1, b1, W2, b2, y1, 1, 4096, 4096, 4096, fm.FMLP_GELU_ERF, ws, ws.numel(), stream=s))
+    assert nk == 2

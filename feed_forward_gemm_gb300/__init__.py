@@ -22,7 +22,7 @@ __all__ = [
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
     "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
-    "fmlp_version", "fmlp_set_tile_policy", "FMLP_TILES_AUTO", "FMLP_TILES_SINGLE",
+    "fmlp_version", "fmlp_set_tile_policy", "fmlp_describe_plan", "FMLP_TILES_AUTO", "FMLP_TILES_SINGLE",
     "FMLP_TILES_PAIR",
     "FMLP_OK", "FMLP_ERR_NULL", "FMLP_ERR_SHAPE", "FMLP_ERR_ALIGN", "FMLP_ERR_ALIAS",
     "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
@@ -63,6 +63,7 @@ _SIGNATURES = {
     "fmlp_last_error": (ctypes.c_char_p, []),
     "fmlp_version": (_INT, []),
     "fmlp_set_tile_policy": (_INT, [_INT]),
+    "fmlp_describe_plan": (_INT, [_INT, _I64, _I64, _I64, _I64, ctypes.c_char_p, _SZ]),
 }
 
 
@@ -206,6 +207,18 @@ def fmlp_linear_plan(T, in_dim, out_dim) -> int:
 def fmlp_gelu_eval(x, out, n, mode=FMLP_GELU_TANH, stream=None, raise_on_error=True):
     st = load().fmlp_gelu_eval(_ptr(x), _ptr(out), n, int(mode), _stream(stream))
     return _check(st, "fmlp_gelu_eval", raise_on_error)
+
+
+PLAN_OPS = {"linear": 0, "linear_gelu": 1, "gate_up": 2, "geglu": 3, "mlp": 4}
+
+
+def fmlp_describe_plan(op, T, D, H, Dout=0) -> str:
+    """The kernels a call with these sizes launches on the current device, as text."""
+    buf = ctypes.create_string_buffer(512)
+    code = PLAN_OPS[op] if isinstance(op, str) else int(op)
+    st = load().fmlp_describe_plan(code, T, D, H, Dout, buf, len(buf))
+    _check(st, "fmlp_describe_plan", True)
+    return buf.value.decode()
 
 
 def fmlp_set_tile_policy(policy: int, raise_on_error=True):

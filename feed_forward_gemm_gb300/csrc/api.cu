@@ -235,16 +235,19 @@ int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu, double* cost_out) {
 // 128x256 single-SM tile with a third less operand traffic, hence its efficiency edge.
 constexpr double kPairEff = 1.15;
 
-fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
-                        const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
-                        int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
-  GemmLaunch L;
-  memset(&L, 0, sizeof L);
+struct GemmChoice {
+  bool pair;   // CTA-pair kernel (256x256 tiles) instead of the single-SM kernel
+  int bn;      // MMA N of the single-SM kernel (256 for the pair kernel)
+  int grid;    // CTAs launched
+};
+
+GemmChoice choose_gemm(const DeviceState& d, int epi, int64_t M, int64_t N_out) {
+  GemmChoice c;
   const bool geglu = epi == EPI_GEGLU;
   double cost1 = 0;
-  L.bn = pick_bn(M, N_out, d.sms, geglu, &cost1);
+  c.bn = pick_bn(M, N_out, d.sms, geglu, &cost1);
+  c.pair = false;
   const int policy = g_tile_policy.load(std::memory_order_relaxed);
-  bool pair = false;
   int pairs = 0;
   if (d.max_pairs >= 1 && M > 128 && policy != FMLP_TILES_SINGLE) {
     const int bn_out2 = geglu ? 128 : 256;
@@ -252,9 +255,28 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
     pairs = static_cast<int>(std::min<int64_t>(tiles2, d.max_pairs));
     const int64_t waves2 = (tiles2 + pairs - 1) / pairs;
     const double cost2 = static_cast<double>(waves2) * 256 / kPairEff;
-    pair = policy == FMLP_TILES_PAIR || cost2 < cost1;
+    c.pair = policy == FMLP_TILES_PAIR || cost2 < cost1;
   }
-  if (pair) L.bn = 256;
+  if (c.pair) {
+    c.bn = 256;
+    c.grid = 2 * pairs;
+  } else {
+    const int bn_out = geglu ? c.bn / 2 : c.bn;
+    const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
+    c.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
+  }
+  return c;
+}
+
+fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
+                        const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
+                        int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
+  GemmLaunch L;
+  memset(&L, 0, sizeof L);
+  const bool geglu = epi == EPI_GEGLU;
+  const GemmChoice ch = choose_gemm(d, epi, M, N_out);
+  const bool pair = ch.pair;
+  L.bn = ch.bn;
   const uint32_t b_rows = pair ? 128u : (geglu ? L.bn / 2 : L.bn);
   FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A"));
   FMLP_TRY(make_map(&L.tmB0, B0, N_out, K, b_rows, "B"));
@@ -274,16 +296,8 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   L.stream = s;
   L.status = d.status;
   L.timeout_ns = kWaitTimeoutNs;
-  cudaError_t e;
-  if (pair) {
-    L.grid = 2 * pairs;
-    e = gemm_tc2_launch(L);
-  } else {
-    const int bn_out = geglu ? L.bn / 2 : L.bn;
-    const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
-    L.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
-    e = gemm_tc_launch(L);
-  }
+  L.grid = ch.grid;
+  const cudaError_t e = pair ? gemm_tc2_launch(L) : gemm_tc_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, pair ? "gemm_tc2 launch" : "gemm_tc launch");
   return FMLP_OK;
 }
@@ -341,6 +355,8 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
   L.gelu_mode = gelu_mode;
   L.grid = static_cast<int>(std::min<int64_t>(N, d.sms));
   L.stream = s;
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
   cudaError_t e = gemv_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
   return FMLP_OK;
@@ -588,6 +604,76 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
   return r;
 }
 
+static std::string describe_gemm(const DeviceState& d, const char* name, int epi, int64_t M,
+                                 int64_t N, int64_t K) {
+  const GemmChoice c = choose_gemm(d, epi, M, N);
+  char b[256];
+  if (c.pair)
+    snprintf(b, sizeof b, "%s: tcgen05 CTA-pair 256x256 tiles, M=%lld N=%lld K=%lld, grid=%d",
+             name, static_cast<long long>(M), static_cast<long long>(N),
+             static_cast<long long>(K), c.grid);
+  else
+    snprintf(b, sizeof b, "%s: tcgen05 single-SM 128x%d tiles, M=%lld N=%lld K=%lld, grid=%d",
+             name, c.bn, static_cast<long long>(M), static_cast<long long>(N),
+             static_cast<long long>(K), c.grid);
+  return b;
+}
+
+static std::string describe_gemv(const DeviceState& d, const char* name, int64_t T, int64_t K,
+                                 int64_t N) {
+  char b[256];
+  snprintf(b, sizeof b, "%s: weight-streaming GEMV, T=%lld K=%lld N=%lld, grid=%lld", name,
+           static_cast<long long>(T), static_cast<long long>(K), static_cast<long long>(N),
+           static_cast<long long>(std::min<int64_t>(N, d.sms)));
+  return b;
+}
+
+fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t Dout, char* buf,
+                               size_t buflen) {
+  t_last_error.clear();
+  if (!buf || buflen == 0) {
+    set_error("buf is NULL or empty");
+    return FMLP_ERR_NULL;
+  }
+  buf[0] = 0;
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  std::string r;
+  if (T <= 0) {
+    r = "nothing launched (T = 0)";
+  } else if (op == 0 || op == 1) {   // linear (+gelu): D -> H
+    const int epi = op == 0 ? EPI_BIAS : EPI_BIAS_GELU;
+    r = plan_linear(T, D, H, d->sms) == FMLP_PLAN_GEMV ? describe_gemv(*d, "linear", T, D, H)
+                                                       : describe_gemm(*d, "linear", epi, T, H, D);
+  } else if (op == 2) {              // gate/up
+    r = gemv_ok(T, D, H, 2, d->sms) ? describe_gemv(*d, "gate/up", T, D, H)
+                                    : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
+  } else if (op == 3) {              // geglu block
+    const int p = plan_geglu(T, D, H, d->sms);
+    if (p == FMLP_PLAN_FUSED_SMALL) {
+      char b[160];
+      snprintf(b, sizeof b, "fused block: one kernel, grid=%lld", static_cast<long long>((T + 127) / 128));
+      r = b;
+    } else if (p == FMLP_PLAN_GEMV) {
+      r = describe_gemv(*d, "gate/up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, D);
+    } else {
+      r = describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
+          describe_gemm(*d, "down", EPI_BIAS, T, D, H);
+    }
+  } else if (op == 4) {              // mlp: D -> H -> Dout
+    if (plan_mlp(T, D, H, Dout, d->sms) == FMLP_PLAN_GEMV)
+      r = describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
+    else
+      r = describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
+          describe_gemm(*d, "down", EPI_BIAS, T, Dout, H);
+  } else {
+    set_error("op %d unknown", op);
+    return FMLP_ERR_SHAPE;
+  }
+  snprintf(buf, buflen, "%s", r.c_str());
+  return FMLP_OK;
+}
+
 fmlp_status fmlp_set_tile_policy(int policy) {
   if (policy != FMLP_TILES_AUTO && policy != FMLP_TILES_SINGLE && policy != FMLP_TILES_PAIR) {
     set_error("tile policy %d unknown", policy);
@@ -634,10 +720,10 @@ fmlp_status fmlp_device_status(fmlp_stream_t s) {
     return cuda_fail(e, "clear device status");
   static const char* sites[] = {"?",          "test wait",          "producer (empty slot)",
                                 "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
-                                "drain",      "fused kernel"};
+                                "drain",      "fused kernel", "GEMV ring"};
   const int site = v >> 8;
   set_error("a kernel gave up waiting at: %s (code 0x%x)",
-            (site >= 0 && site < 8) ? sites[site] : "?", v);
+            (site >= 0 && site < 9) ? sites[site] : "?", v);
   return static_cast<fmlp_status>(v & 0xFF);
 }
 

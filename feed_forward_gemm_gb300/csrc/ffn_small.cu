@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 
 cudaError_t ffn_small_launch(const SmallLaunch& L) {
   const int smem = ffn_small_smem_bytes(L.D);
-  cudaError_t e =
-      cudaFuncSetAttribute(ffn_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static SmemAttrCache cache;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(ffn_small_kernel), smem, cache);
   if (e != cudaSuccess) return e;
   const int grid = (L.T + 127) / 128;
   ffn_small_kernel<<<grid, kSmallThreads, smem, L.stream>>>(L.tmX, L.tmWg, L.tmWu, L.tmWd, L.tmY,

@@ -250,9 +250,8 @@ template <int BN, int EPI>
 static cudaError_t launch_one(const GemmLaunch& L) {
   using C = Cfg<BN, EPI>;
   auto kern = gemm_tc_kernel<BN, EPI>;
-  // The attribute is per function and device; setting it is cheap and idempotent.
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  static SmemAttrCache cache;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, cache);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid, 1, 1);

@@ -240,8 +240,8 @@ int gemm_tc2_smem_bytes() { return kPairSmem; }
 template <int EPI>
 static cudaError_t launch_pair(const GemmLaunch& L) {
   auto kern = gemm_tc2_kernel<EPI>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  static SmemAttrCache cache;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kPairSmem, cache);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid, 1, 1);

@@ -1,43 +1,52 @@
 // Weight-streaming GEMV for a few tokens (decode): y[t, n] = epi(sum_k x[t, k] W[n, k] (+ b[n])).
 //
-// At one token the feed-forward block reads every weight once and does two flops per weight
-// byte pair, so it is bound by HBM bandwidth and by launch latency (ainews.cool fused-MLP
-// article, technical deep-dive: batch-1 decode pays one launch per layer). The kernel is
-// built for that:
+// At one token the feed-forward block reads every weight once and does one multiply-add per
+// weight, so it is bound by HBM bandwidth and by launch latency (ainews.cool fused-MLP
+// article, technical deep-dive: batch-1 decode pays one launch per layer and is limited by
+// memory traffic). The kernel is built for that:
 //   - each CTA owns a contiguous block of weight rows [r0, r1) (balanced to +-1 row), so the
-//     bytes it streams are one contiguous range of W;
-//   - a row is cut into 512-byte segments (256 bf16, one 16-byte load per lane); warp w of
-//     the CTA takes segments w, w+16, w+32, ... and keeps 8 of them (4 KB) in flight per
-//     batch with non-allocating 128-bit loads;
-//   - x (T x K bf16) sits in shared memory; each segment's dot product is reduced with warp
-//     shuffles in fp32, the per-segment partials go to shared memory, and one thread per
-//     (row, token) adds them in segment order (deterministic) and applies the epilogue;
-//   - with two weight matrices (GeGLU gate and up) both are streamed and the epilogue forms
-//     gelu_tanh(g) * u;
-//   - programmatic dependent launch: the kernel lets the next kernel launch at once, prefetches
-//     its own weight range into L2 and only then waits for the previous kernel, so one layer's
-//     weight stream overlaps the previous layer's tail and launch.
+//     bytes it streams form one contiguous range per weight matrix;
+//   - one producer warp streams that range through a ring of 16 KB shared-memory slots with
+//     1-D bulk async copies (cp.async.bulk, completion counted on an mbarrier), keeping up to
+//     eight slots - 128 KB per SM - in flight; no register file is spent on loads in flight;
+//   - a slot is 32 segments of 512 bytes (one 16-byte vector per lane, 256 weights of one
+//     row); eight compute warps take four segments each, form the dot product with x (held
+//     in shared memory) in fp32, reduce it with warp shuffles and store one partial per
+//     (row, segment); one thread per (row, token) then adds a row's partials in segment
+//     order (deterministic) and applies the epilogue;
+//   - with two weight matrices (GeGLU gate and up) both ranges are streamed and the epilogue
+//     forms gelu_tanh(g) * u;
+//   - programmatic dependent launch: the kernel lets the next kernel launch at once and
+//     prefetches its whole weight range into L2 before waiting for the previous kernel, so a
+//     layer's weights stream in while the previous layer finishes.
+// Every wait is bounded.
 #include "activation.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fmlp {
 
-constexpr int kGemvThreads = 512;
-constexpr int kGemvWarps = kGemvThreads / 32;
-constexpr int kGemvBatch = 8;
-constexpr int kSeg = 256;  // elements per segment
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kGemvComputeWarps = 8;
+constexpr int kGemvThreads = (kGemvComputeWarps + 1) * 32;  // + one producer warp
+constexpr int kSeg = 256;                                    // weights per segment
+constexpr int kSegBytes = kSeg * 2;
+constexpr int kSlotSegs = 32;
+constexpr int kSlotBytes = kSlotSegs * kSegBytes;            // 16 KB
+constexpr int kMaxSlots = 8;
+constexpr int kMinSlots = 2;
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
@@ -52,82 +61,145 @@ __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
   return s;
 }
 
+struct GemvSmem {
+  size_t x_off, part_off, ring_off, bar_off, total;
+  int slots;
+};
+
+__host__ __device__ inline GemvSmem gemv_layout(int T, int K, int rows_max, int nmat,
+                                                size_t budget) {
+  GemvSmem L;
+  L.x_off = 0;
+  const size_t xb = static_cast<size_t>(T) * K * 2;
+  L.part_off = (xb + 15) & ~size_t(15);
+  const size_t pb = static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+  L.ring_off = (L.part_off + pb + 1023) & ~size_t(1023);
+  const size_t fixed = L.ring_off + 2 * kMaxSlots * 8 + 1024;
+  int slots = kMinSlots;
+  if (budget > fixed) {
+    const size_t s = (budget - fixed) / kSlotBytes;
+    slots = s > kMaxSlots ? kMaxSlots : (s < kMinSlots ? kMinSlots : static_cast<int>(s));
+  }
+  L.slots = slots;
+  L.bar_off = L.ring_off + static_cast<size_t>(slots) * kSlotBytes;
+  L.total = L.bar_off + 2 * kMaxSlots * 8 + 1024;  // + alignment slack for the base
+  return L;
+}
+
 template <int EPI, int NMAT, int TMAX>
-__global__ void __launch_bounds__(kGemvThreads, 2)
+__global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
                 const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode) {
-  extern __shared__ __align__(16) uint8_t gsm[];
-  const int rows_total = N;
-  const int r0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * rows_total) / gridDim.x);
-  const int r1 =
-      static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * rows_total) / gridDim.x);
+                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode,
+                int rows_max, int slots, int* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t gsm_raw[];
+  uint8_t* gsm = gsm_raw + ((1024u - (smem_u32(gsm_raw) & 1023u)) & 1023u);
+  const GemvSmem Ly = gemv_layout(T, K, rows_max, NMAT, 0);  // offsets only (slots from host)
+  const int r0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * N) / gridDim.x);
+  const int r1 = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * N) / gridDim.x);
   const int rows = r1 - r0;
   const int segs = K / kSeg;
-  const int per_mat = rows * segs;
-  const int ntask = NMAT * per_mat;
+  const int per_mat = rows * segs;                                   // segments per matrix
+  const int chunks_per_mat = (per_mat + kSlotSegs - 1) / kSlotSegs;
+  const int nchunks = NMAT * chunks_per_mat;
 
-  uint4* xs = reinterpret_cast<uint4*>(gsm);                        // [T][K/8]
-  float* part = reinterpret_cast<float*>(gsm + static_cast<size_t>(T) * K * 2);  // [task][T]
+  uint4* xs = reinterpret_cast<uint4*>(gsm + Ly.x_off);              // [T][K/8]
+  float* part = reinterpret_cast<float*>(gsm + Ly.part_off);         // [mat][row][seg][T]
+  uint8_t* ring = gsm + Ly.ring_off;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(slots) * kSlotBytes);
+  uint64_t* empty = full + kMaxSlots;
 
-  if (threadIdx.x == 0) pdl_launch_dependents();
-  // Warm L2 with this CTA's weight rows; they do not depend on the previous kernel.
-  if (threadIdx.x < NMAT) {
-    const __nv_bfloat16* Wm = threadIdx.x == 0 ? W0 : W1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kGemvComputeWarps);
+    }
+    fence_mbarrier_init();
+    pdl_launch_dependents();
+  }
+  // Warm L2 with this CTA's weight rows; they are not produced by the previous kernel.
+  if (warp == kGemvComputeWarps && lane < NMAT) {
+    const __nv_bfloat16* Wm = lane == 0 ? W0 : W1;
     const char* base = reinterpret_cast<const char*>(Wm + static_cast<size_t>(r0) * K);
-    size_t bytes = static_cast<size_t>(rows) * K * 2;
+    const size_t bytes = static_cast<size_t>(rows) * K * 2;
     for (size_t off = 0; off < bytes; off += 65536) {
       const size_t n = bytes - off < 65536 ? bytes - off : 65536;
       prefetch_l2_bulk(base + off, static_cast<uint32_t>(n));
     }
   }
+  __syncthreads();
   pdl_wait_primary();
 
-  // x -> shared memory
-  const int xvec = T * (K / 8);
-  for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
-    xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
-  __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int base = warp; base < ntask; base += kGemvWarps * kGemvBatch) {
-    uint4 wv[kGemvBatch];
-#pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int q = base + u * kGemvWarps;
-      if (q < ntask) {
-        const int mat = NMAT == 2 ? (q >= per_mat ? 1 : 0) : 0;
-        const int rem = q - mat * per_mat;
-        const int row = rem / segs, seg = rem - row * segs;
+  if (warp == kGemvComputeWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t issued = 0, last_par = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % slots;
+        const uint32_t par = static_cast<uint32_t>(c / slots) & 1u;
+        if (!mbar_wait(&empty[s], par ^ 1u, status, SITE_GEMV, timeout_ns)) break;
+        const int mat = NMAT == 2 ? c / chunks_per_mat : 0;
+        const int cm = c - mat * chunks_per_mat;
+        const int seg0 = cm * kSlotSegs;
+        const int nseg = per_mat - seg0 < kSlotSegs ? per_mat - seg0 : kSlotSegs;
         const __nv_bfloat16* Wm = mat ? W1 : W0;
-        wv[u] = ld_stream_v4(Wm + static_cast<size_t>(r0 + row) * K + seg * kSeg + lane * 8);
-      } else {
-        wv[u] = make_uint4(0u, 0u, 0u, 0u);
+        const char* src = reinterpret_cast<const char*>(Wm + static_cast<size_t>(r0) * K) +
+                          static_cast<size_t>(seg0) * kSegBytes;
+        const uint32_t bytes = static_cast<uint32_t>(nseg) * kSegBytes;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(ring + static_cast<size_t>(s) * kSlotBytes, src, bytes, &full[s]);
+        issued |= 1u << s;
+        last_par = (last_par & ~(1u << s)) | (par << s);
       }
+      // every copy issued must land before the CTA can exit (normally consumed already)
+      for (int s = 0; s < slots; ++s)
+        if (issued & (1u << s))
+          mbar_wait(&full[s], (last_par >> s) & 1u, status, SITE_DRAIN, timeout_ns);
     }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int xvec = T * (K / 8);
+    for (int i = threadIdx.x; i < xvec; i += kGemvComputeWarps * 32)
+      xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    asm volatile("bar.sync 1, %0;" ::"n"(kGemvComputeWarps * 32) : "memory");
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % slots;
+      const uint32_t par = static_cast<uint32_t>(c / slots) & 1u;
+      const bool ok = mbar_wait(&full[s], par, status, SITE_GEMV, timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int mat = NMAT == 2 ? c / chunks_per_mat : 0;
+      const int cm = c - mat * chunks_per_mat;
+      const int seg0 = cm * kSlotSegs;
+      const uint8_t* slot = ring + static_cast<size_t>(s) * kSlotBytes;
 #pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int q = base + u * kGemvWarps;
-      if (q >= ntask) break;  // warp-uniform
-      const int mat = NMAT == 2 ? (q >= per_mat ? 1 : 0) : 0;
-      const int rem = q - mat * per_mat;
-      const int seg = rem % segs;
-      float p[TMAX];
+      for (int j = warp; j < kSlotSegs; j += kGemvComputeWarps) {
+        const int g = seg0 + j;   // segment index within this matrix block
+        if (g < per_mat) {        // warp-uniform
+          const int row = g / segs, seg = g - row * segs;
+          const uint4 wv = *reinterpret_cast<const uint4*>(slot + j * kSegBytes + lane * 16);
+          float p[TMAX];
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        p[t] = 0.f;
-        if (t < T) p[t] = dot8(wv[u], xs[t * (K / 8) + seg * (kSeg / 8) + lane]);
+          for (int t = 0; t < TMAX; ++t) {
+            p[t] = 0.f;
+            if (t < T) p[t] = dot8(wv, xs[t * (K / 8) + seg * (kSeg / 8) + lane]);
+          }
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) p[t] += __shfl_xor_sync(0xffffffffu, p[t], o);
+          }
+          if (lane == 0) {
+            const size_t pi = (static_cast<size_t>(mat) * per_mat + row * segs + seg) * T;
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t)
+              if (t < T) part[pi + t] = p[t];
+          }
+        }
       }
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) p[t] += __shfl_xor_sync(0xffffffffu, p[t], o);
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t)
-          if (t < T) part[static_cast<size_t>(q) * T + t] = p[t];
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
   __syncthreads();
@@ -153,21 +225,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
-  const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
-  return static_cast<size_t>(T) * K * 2 +
-         static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+  const int rows_max = static_cast<int>((static_cast<int64_t>(N) + grid - 1) / grid);
+  return gemv_layout(T, K, rows_max, nmat, kGemvPreferSmem).total;
 }
 
 template <int EPI, int NMAT, int TMAX>
-static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
+static cudaError_t gemv_launch_t(const GemvLaunch& L, const GemvSmem& lay, int rows_max) {
   auto kern = gemv_kernel<EPI, NMAT, TMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static SmemAttrCache cache;
+  cudaError_t e =
+      set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(lay.total), cache);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = lay.total;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -178,25 +250,27 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
                             static_cast<const __nv_bfloat16*>(L.W0),
                             static_cast<const __nv_bfloat16*>(L.W1),
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode,
+                            rows_max, lay.slots, L.status, L.timeout_ns);
 }
 
 cudaError_t gemv_launch(const GemvLaunch& L) {
   const int nmat = L.epi == EPI_GEGLU ? 2 : 1;
-  const size_t smem = gemv_smem_bytes(L.T, L.K, L.N, nmat, L.grid);
-  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || smem > kGemvMaxSmem)
-    return cudaErrorInvalidValue;
+  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || L.grid < 1) return cudaErrorInvalidValue;
+  const int rows_max = static_cast<int>((static_cast<int64_t>(L.N) + L.grid - 1) / L.grid);
+  const GemvSmem lay = gemv_layout(L.T, L.K, rows_max, nmat, kGemvPreferSmem);
+  if (lay.total > kGemvMaxSmem) return cudaErrorInvalidValue;
   if (L.T == 1) {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1>(L, smem);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1>(L, smem);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1>(L, smem);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1>(L, lay, rows_max);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1>(L, lay, rows_max);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1>(L, lay, rows_max);
     }
   } else {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT>(L, smem);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT>(L, smem);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT>(L, smem);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT>(L, lay, rows_max);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT>(L, lay, rows_max);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT>(L, lay, rows_max);
     }
   }
   return cudaErrorInvalidValue;

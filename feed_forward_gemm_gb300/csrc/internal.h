@@ -6,7 +6,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fmlp {
+
+// Raises a kernel's dynamic shared-memory limit on the current device only when a call needs
+// more than was set before (one cudaFuncSetAttribute per kernel and device in practice).
+// Each launch site keeps its own cache object.
+struct SmemAttrCache {
+  std::atomic<int> bytes[64] = {};
+};
+
+inline cudaError_t set_smem_limit(const void* kern, int bytes, SmemAttrCache& cache) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && cache.bytes[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) {
+    int cur = cache.bytes[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !cache.bytes[dev].compare_exchange_weak(cur, bytes)) {
+    }
+  }
+  return e;
+}
 
 // Epilogue kinds of the tcgen05 GEMM.
 enum Epi : int {
@@ -44,7 +68,11 @@ int gemm_tc_smem_bytes(int epi, int bn);
 
 // Weight-streaming GEMV for T <= kGemvMaxT tokens (decode).
 constexpr int kGemvMaxT = 4;
-constexpr size_t kGemvMaxSmem = 100 * 1024;  // two CTAs per SM for launch overlap
+// Shared memory: the ring of weight slots is sized to fit kGemvPreferSmem (two CTAs per SM, so
+// the next layer's CTAs can start while this layer runs); shapes whose x and partial sums need
+// more may use up to kGemvMaxSmem with the minimum ring.
+constexpr size_t kGemvPreferSmem = 112 * 1024;
+constexpr size_t kGemvMaxSmem = 200 * 1024;
 struct GemvLaunch {
   const void* x;      // [T, K]
   const void* W0;     // [N, K]  (Wg for GeGLU)
@@ -56,6 +84,8 @@ struct GemvLaunch {
   int gelu_mode;
   int grid;
   cudaStream_t stream;
+  int* status;
+  uint64_t timeout_ns;
 };
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);
 cudaError_t gemv_launch(const GemvLaunch& L);

@@ -20,6 +20,7 @@ enum WaitSite : int {
   SITE_EPI_TMEM_FULL = 5,
   SITE_DRAIN = 6,
   SITE_SMALL = 7,
+  SITE_GEMV = 8,
 };
 constexpr int kDeviceTimeoutCode = 7;  // FMLP_ERR_DEVICE_TIMEOUT
 

@@ -140,6 +140,13 @@ FMLP_API int fmlp_linear_plan(int64_t T, int64_t in, int64_t out);
 typedef enum { FMLP_TILES_AUTO = 0, FMLP_TILES_SINGLE = 1, FMLP_TILES_PAIR = 2 } fmlp_tile_policy;
 FMLP_API fmlp_status fmlp_set_tile_policy(int policy);
 
+/* Writes a one-line description of the kernels a call with these sizes would launch on the
+ * current device (tile kernel, tile shape, grid) into buf (NUL-terminated, truncated to
+ * buflen). op: 0 fmlp_linear_bias (in = D, out = H), 1 fmlp_linear_bias_gelu (same),
+ * 2 fmlp_geglu_gate_up, 3 fmlp_geglu, 4 fmlp_mlp_gelu. Launches nothing. */
+FMLP_API fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t Dout,
+                                        char* buf, size_t buflen);
+
 /* Device activation check: out[i] = GELU(in[i]) in fp32 with the exact device code the
  * epilogues use. in/out: n floats in device memory. One kernel. */
 FMLP_API fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,

@@ -9,7 +9,7 @@ import torch
 import feed_forward_gemm_gb300 as fm
 import oracle
 import synth
-from gpu_util import DEV, empty_bf16, guarded_bf16, to_dev, to_host, workspace
+from gpu_util import DEV, count_graph_kernels, empty_bf16, guarded_bf16, to_dev, to_host, workspace
 from helpers import assert_parity, rne_bf16_array
 
 pytestmark = pytest.mark.gpu
@@ -137,56 +137,32 @@ def test_gemv_deterministic_across_calls():
 
 # ------------------------------------------------------------------------ kernel counts
 
-def count_kernels_in_graph(fn):
-    from cuda.bindings import runtime as rt
-    s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        fn(s)
-    torch.cuda.synchronize()
-    err, = rt.cudaStreamBeginCapture(s.cuda_stream, rt.cudaStreamCaptureMode.cudaStreamCaptureModeThreadLocal)[:1]
-    assert err == rt.cudaError_t.cudaSuccess
-    fn(s)
-    err, graph = rt.cudaStreamEndCapture(s.cuda_stream)
-    assert err == rt.cudaError_t.cudaSuccess
-    err, _, n = rt.cudaGraphGetNodes(graph, 0)
-    assert err == rt.cudaError_t.cudaSuccess
-    err, nodes, n = rt.cudaGraphGetNodes(graph, n)
-    kinds = []
-    for node in nodes[:n]:
-        err, ty = rt.cudaGraphNodeGetType(node)
-        kinds.append(ty)
-    rt.cudaGraphDestroy(graph)
-    return sum(1 for k in kinds if k == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel), len(kinds)
-
-
 @pytest.mark.parametrize("T,D,H,plan,kernels", [
     (1024, 32, 64, fm.FMLP_PLAN_FUSED_SMALL, 1),
     (1, 768, 3072, fm.FMLP_PLAN_GEMV, 2),
     (512, 768, 3072, fm.FMLP_PLAN_TC, 2),
 ])
 def test_geglu_kernel_count(T, D, H, plan, kernels):
-    pytest.importorskip("cuda.bindings")
     assert fm.fmlp_geglu_plan(T, D, H) == plan
     x, Wg, Wu, Wd = (to_dev(a) for a in geglu_inputs(T, D, H))
     y = empty_bf16(T, D)
     ws = workspace(fm.fmlp_geglu_workspace_size(T, D, H))
-    nk, nall = count_kernels_in_graph(
+    nk, nall = count_graph_kernels(
         lambda s: fm.fmlp_geglu(x, Wg, Wu, Wd, y, T, D, H, ws, ws.numel(), stream=s))
     assert nk == kernels and nall == kernels
 
 
 def test_linear_and_mlp_kernel_counts():
-    pytest.importorskip("cuda.bindings")
     T, K, N = 1024, 32, 64
     x, W, b = to_dev(rbits((T, K))), to_dev(ubits((N, K), .1)), to_dev(ubits((N,), .1))
     y = empty_bf16(T, N)
-    nk, _ = count_kernels_in_graph(lambda s: fm.fmlp_linear_bias(x, W, b, y, T, K, N, stream=s))
+    nk, _ = count_graph_kernels(lambda s: fm.fmlp_linear_bias(x, W, b, y, T, K, N, stream=s))
     assert nk == 1     # the bias add is the GEMM's epilogue: one kernel
     x1 = to_dev(rbits((1, 4096)))
     W1, W2 = to_dev(ubits((4096, 4096), 1 / 64)), to_dev(ubits((4096, 4096), 1 / 64))
     b1, b2 = to_dev(ubits((4096,), 1 / 64)), to_dev(ubits((4096,), 1 / 64))
     y1 = empty_bf16(1, 4096)
     ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, 4096, 4096, 4096))
-    nk, _ = count_kernels_in_graph(lambda s: fm.fmlp_mlp_gelu(
+    nk, _ = count_graph_kernels(lambda s: fm.fmlp_mlp_gelu(
         x1, W1, b1, W2, b2, y1, 1, 4096, 4096, 4096, fm.FMLP_GELU_ERF, ws, ws.numel(), stream=s))
     assert nk == 2

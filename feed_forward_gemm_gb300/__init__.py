@@ -22,7 +22,7 @@ __all__ = [
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
     "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
-    "fmlp_version", "fmlp_set_tile_policy", "fmlp_describe_plan", "FMLP_TILES_AUTO", "FMLP_TILES_SINGLE",
+    "fmlp_version", "fmlp_set_tile_policy", "fmlp_describe_plan", "fmlp_geglu_noalloc", "FMLP_TILES_AUTO", "FMLP_TILES_SINGLE",
     "FMLP_TILES_PAIR",
     "FMLP_OK", "FMLP_ERR_NULL", "FMLP_ERR_SHAPE", "FMLP_ERR_ALIGN", "FMLP_ERR_ALIAS",
     "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
@@ -64,6 +64,7 @@ _SIGNATURES = {
     "fmlp_version": (_INT, []),
     "fmlp_set_tile_policy": (_INT, [_INT]),
     "fmlp_describe_plan": (_INT, [_INT, _I64, _I64, _I64, _I64, ctypes.c_char_p, _SZ]),
+    "fmlp_geglu_noalloc": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
 }
 
 
@@ -175,6 +176,14 @@ def fmlp_geglu(x, Wg, Wu, Wd, y, T, D, H, ws=None, ws_bytes=0, stream=None,
     st = load().fmlp_geglu(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(y), T, D, H, _ptr(ws),
                            int(ws_bytes), _stream(stream))
     return _check(st, "fmlp_geglu", raise_on_error)
+
+
+def fmlp_geglu_noalloc(x, Wg, Wu, Wd, y, T, D, H, stream=None, raise_on_error=True):
+    """fmlp_geglu with the intermediate in the library's fixed device array (allocates
+    nothing; T*H*2 bytes must fit in 64 MiB; overlapping calls race on the array)."""
+    st = load().fmlp_geglu_noalloc(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(y), T, D, H,
+                                   _stream(stream))
+    return _check(st, "fmlp_geglu_noalloc", raise_on_error)
 
 
 def fmlp_mlp_gelu(x, W1, b1, W2, b2, y, T, D, H, Dout, mode=FMLP_GELU_ERF, ws=None, ws_bytes=0,

@@ -384,6 +384,16 @@ fmlp_status launch_small(const DeviceState& d, const void* x, const void* Wg, co
 }
 
 }  // namespace
+
+void record_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+}
+
 }  // namespace fmlp
 
 using namespace fmlp;

@@ -107,6 +107,9 @@ struct SmallLaunch {
 int ffn_small_smem_bytes(int D);
 cudaError_t ffn_small_launch(const SmallLaunch& L);
 
+// Records the calling thread's fmlp_last_error() text (printf-style).
+void record_error(const char* fmt, ...);
+
 // Device GELU check kernel.
 cudaError_t gelu_eval_launch(const float* in, float* out, int64_t n, int mode,
                              cudaStream_t stream);

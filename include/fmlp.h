@@ -123,6 +123,28 @@ FMLP_API fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1
                           int64_t Dout, fmlp_gelu_mode mode, void* ws, size_t ws_bytes,
                           fmlp_stream_t s);
 
+/* fmlp_geglu for callers that cannot allocate device memory (no counterpart in the pages).
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocating routine - a plugin in a
+ * serving process whose memory pool owns the device, a real-time loop that must not risk an
+ * allocation stall or failure, work being recorded into a CUDA graph. fmlp_geglu keeps the
+ * intermediate m in a caller workspace (or allocates one); this call keeps it in a fixed
+ * 64 MiB array of device memory that belongs to the library, and allocates nothing: it
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, layouts and results as fmlp_geglu without ws/ws_bytes. Limit:
+ * fmlp_geglu_workspace_size(T, D, H) <= 64 MiB (e.g. T*H <= 32M); larger sizes return
+ * FMLP_ERR_WORKSPACE without launching anything. Every GPU that loads the library holds the
+ * 64 MiB array until the process exits. All calls share the array (it keeps the last call's
+ * m; every call overwrites all of m it reads, so nothing needs clearing): calls whose kernels
+ * can overlap on the GPU - on different streams, or from different threads without ordering -
+ * race on it and must be serialised by the caller. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture on the device. */
+FMLP_API fmlp_status fmlp_geglu_noalloc(const void* x, const void* Wg, const void* Wu,
+                                        const void* Wd, void* y, int64_t T, int64_t D, int64_t H,
+                                        fmlp_stream_t s);
+
 /* Workspace bytes the calls above need (T*H*2 for the 2-kernel plans, else 0). Pure host
  * functions; they touch no device. */
 FMLP_API size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H);

@@ -48,6 +48,8 @@ def parse():
                         "inputs of --shape and exit (no timing, no JSON)")
     p.add_argument("--shape", default="8192,8192,8192", help="T,D,H for --profile-kernel")
     p.add_argument("--launches", type=int, default=3)
+    p.add_argument("--tiles", default="auto", choices=["auto", "single", "pair"],
+                   help="tile-kernel policy for --profile-kernel")
     return p.parse_args()
 
 
@@ -529,6 +531,8 @@ def run_profile_case(args):
     mid = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
     k = args.profile_kernel
+    fm.fmlp_set_tile_policy({"auto": fm.FMLP_TILES_AUTO, "single": fm.FMLP_TILES_SINGLE,
+                             "pair": fm.FMLP_TILES_PAIR}[args.tiles])
     for _ in range(args.launches):
         if k == "gate_up":
             fm.fmlp_geglu_gate_up(x, W1, W2, mid, T, D, H)
@@ -547,7 +551,7 @@ def run_profile_case(args):
     st = fm.fmlp_device_status()
     if st != fm.FMLP_OK:
         raise SystemExit(f"device status {st}: {fm.fmlp_last_error()}")
-    print(f"profile case {k} {T}x{D}x{H}: {args.launches} launches ok")
+    print(f"profile case {k} {T}x{D}x{H} tiles={args.tiles}: {args.launches} launches ok")
 
 
 def main():

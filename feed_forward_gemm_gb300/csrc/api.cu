@@ -233,7 +233,7 @@ int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu, double* cost_out) {
 
 // The CTA-pair kernel computes 256x256 tiles with two SMs; per SM that is the work of one
 // 128x256 single-SM tile with a third less operand traffic, hence its efficiency edge.
-constexpr double kPairEff = 1.15;
+constexpr double kPairEff = 1.3;
 
 struct GemmChoice {
   bool pair;   // CTA-pair kernel (256x256 tiles) instead of the single-SM kernel
@@ -310,7 +310,8 @@ constexpr int kPlanSms = 152;
 
 bool gemv_ok(int64_t T, int64_t K, int64_t N, int nmat, int sms) {
   if (T < 1 || T > kGemvMaxT || K % 256 != 0) return false;
-  const int grid = static_cast<int>(std::min<int64_t>(N, sms));
+  const int grid = gemv_grid(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), nmat,
+                             sms);
   return gemv_smem_bytes(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), nmat,
                          grid) <= kGemvMaxSmem;
 }
@@ -353,10 +354,9 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
   L.N = static_cast<int>(N);
   L.epi = epi;
   L.gelu_mode = gelu_mode;
-  L.grid = static_cast<int>(std::min<int64_t>(N, d.sms));
+  L.grid = gemv_grid(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N),
+                     epi == EPI_GEGLU ? 2 : 1, d.sms);
   L.stream = s;
-  L.status = d.status;
-  L.timeout_ns = kWaitTimeoutNs;
   cudaError_t e = gemv_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
   return FMLP_OK;
@@ -630,11 +630,12 @@ static std::string describe_gemm(const DeviceState& d, const char* name, int epi
 }
 
 static std::string describe_gemv(const DeviceState& d, const char* name, int64_t T, int64_t K,
-                                 int64_t N) {
+                                 int64_t N, int nmat = 1) {
   char b[256];
   snprintf(b, sizeof b, "%s: weight-streaming GEMV, T=%lld K=%lld N=%lld, grid=%lld", name,
            static_cast<long long>(T), static_cast<long long>(K), static_cast<long long>(N),
-           static_cast<long long>(std::min<int64_t>(N, d.sms)));
+           static_cast<long long>(gemv_grid(static_cast<int>(T), static_cast<int>(K),
+                                            static_cast<int>(N), nmat, d.sms)));
   return b;
 }
 
@@ -656,7 +657,7 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
     r = plan_linear(T, D, H, d->sms) == FMLP_PLAN_GEMV ? describe_gemv(*d, "linear", T, D, H)
                                                        : describe_gemm(*d, "linear", epi, T, H, D);
   } else if (op == 2) {              // gate/up
-    r = gemv_ok(T, D, H, 2, d->sms) ? describe_gemv(*d, "gate/up", T, D, H)
+    r = gemv_ok(T, D, H, 2, d->sms) ? describe_gemv(*d, "gate/up", T, D, H, 2)
                                     : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
   } else if (op == 3) {              // geglu block
     const int p = plan_geglu(T, D, H, d->sms);
@@ -665,7 +666,7 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       snprintf(b, sizeof b, "fused block: one kernel, grid=%lld", static_cast<long long>((T + 127) / 128));
       r = b;
     } else if (p == FMLP_PLAN_GEMV) {
-      r = describe_gemv(*d, "gate/up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, D);
+      r = describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
     } else {
       r = describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
           describe_gemm(*d, "down", EPI_BIAS, T, D, H);
@@ -730,7 +731,7 @@ fmlp_status fmlp_device_status(fmlp_stream_t s) {
     return cuda_fail(e, "clear device status");
   static const char* sites[] = {"?",          "test wait",          "producer (empty slot)",
                                 "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
-                                "drain",      "fused kernel", "GEMV ring"};
+                                "drain",      "fused kernel", "GEMV"};
   const int site = v >> 8;
   set_error("a kernel gave up waiting at: %s (code 0x%x)",
             (site >= 0 && site < 9) ? sites[site] : "?", v);

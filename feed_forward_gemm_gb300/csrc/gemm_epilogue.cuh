@@ -1,12 +1,17 @@
-// Epilogue of the tcgen05 GEMM kernels: one warp turns its 32 TMEM lanes (32 output rows)
-// of a finished accumulator into bf16 output tiles.
+// Epilogue of the tcgen05 GEMM kernels: one warp turns its 32 TMEM lanes (32 output rows) of a
+// finished accumulator into bf16 output tiles.
+//
+// Four epilogue warps share a tile: warp w reads TMEM lanes [32(w%4), 32(w%4)+32) (the quarter
+// its position in the CTA allows) and all of the tile's output columns. (Eight warps with half
+// the columns each were measured slower: they take issue slots from the single thread that
+// issues the MMAs.)
 //
 // For each 64-column output chunk the warp loads the fp32 accumulator 32 columns at a time
-// (tcgen05.ld 32x32b.x32: lane i holds row i), applies the epilogue, rounds once to bf16,
-// writes the row into a 32x128-byte staging tile in the 128-byte swizzled layout (16-byte
-// chunk j of row r goes to slot j ^ (r & 7), so eight consecutive lanes hit eight different
-// bank groups) and lane 0 stores the tile with one TMA store. Two staging tiles alternate so
-// the store of one chunk overlaps the math of the next.
+// (tcgen05.ld 32x32b.x32: lane i holds row i), applies the epilogue in place, rounds once to
+// bf16, writes the row into a 32x128-byte staging tile in the 128-byte swizzled layout
+// (16-byte chunk j of row r goes to slot j ^ (r & 7), so eight consecutive lanes hit eight
+// different bank groups) and lane 0 stores the tile with one TMA store. Two staging tiles
+// alternate so the store of one chunk overlaps the math of the next.
 //   EPI_BIAS       v = acc + b
 //   EPI_BIAS_GELU  v = gelu(acc + b)
 //   EPI_GEGLU      v = gelu_tanh(acc[c]) * acc[c + BN/2]  (gate columns, then up columns)
@@ -19,79 +24,80 @@
 namespace fmlp {
 
 constexpr int kStgBytes = 32 * 128;  // one staging tile: 32 rows x 64 bf16
+constexpr int kEpiWarps = 4;
+constexpr int kStgPerWarp = 2;       // staging tiles per epilogue warp (double buffer)
 
+// stg: this warp's kStgPerWarp staging tiles; sb: which one is next (kept across tiles).
 template <int BN, int BN_OUT, int EPI>
-__device__ __forceinline__ void epilogue_rows(uint32_t t_row, uint8_t* stg, int& sb, int lane,
-                                              int row0, int n_tile0, int M, int N_out,
-                                              const CUtensorMap* tmY,
+__device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base, int& sb,
+                                              int lane, int row0, int n_tile0, int M,
+                                              int N_out, const CUtensorMap* tmY,
                                               const __nv_bfloat16* __restrict__ bias,
                                               int gelu_mode) {
 #pragma unroll 1
-  for (int ch = 0; ch < BN_OUT / 64; ++ch) {
-    const int n_chunk = n_tile0 + ch * 64;
-    uint8_t* sbuf = stg + sb * kStgBytes;
-    // the TMA store that last read this staging buffer must be done reading it
-    if (lane == 0) bulk_wait_group_read<1>();
+  for (int ch = 0; ch < BN_OUT; ch += 64) {
+    const int n_chunk = n_tile0 + ch;
+    uint8_t* stg = stg_base + sb * kStgBytes;
+    // the TMA store that last read this staging tile must be done reading it
+    if (lane == 0) bulk_wait_group_read<kStgPerWarp - 1>();
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int c = ch * 64 + h * 32;
-      uint32_t acc[32];
-      tmem_ld_32x32b_x32(t_row + c, acc);
-      float v[32];
+      const int c = ch + h * 32;
+      uint32_t a[32];
+      tmem_ld_32x32b_x32(t_row + c, a);
       if (EPI == EPI_GEGLU) {
-        uint32_t up[32];
-        tmem_ld_32x32b_x32(t_row + BN / 2 + c, up);
+        uint32_t u[32];
+        tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          v[i] = gelu_tanh_f(__uint_as_float(acc[i])) * __uint_as_float(up[i]);
+          a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])) * __uint_as_float(u[i]));
       } else {
         tmem_ld_wait();
-        float bv[32];
         const int nb = n_chunk + h * 32;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 w = make_uint4(0u, 0u, 0u, 0u);
           if (bias != nullptr && nb + q * 8 < N_out)
             w = __ldg(reinterpret_cast<const uint4*>(bias + nb + q * 8));
-          bv[q * 8 + 0] = bf16_lo(w.x);
-          bv[q * 8 + 1] = bf16_hi(w.x);
-          bv[q * 8 + 2] = bf16_lo(w.y);
-          bv[q * 8 + 3] = bf16_hi(w.y);
-          bv[q * 8 + 4] = bf16_lo(w.z);
-          bv[q * 8 + 5] = bf16_hi(w.z);
-          bv[q * 8 + 6] = bf16_lo(w.w);
-          bv[q * 8 + 7] = bf16_hi(w.w);
-        }
+          const uint32_t wb[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float z = __uint_as_float(acc[i]) + bv[i];
-          v[i] = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
+          for (int e = 0; e < 4; ++e) {
+            const int i = q * 8 + e * 2;
+            float z0 = __uint_as_float(a[i]) + bf16_lo(wb[e]);
+            float z1 = __uint_as_float(a[i + 1]) + bf16_hi(wb[e]);
+            if (EPI == EPI_BIAS_GELU) {
+              z0 = gelu_f(z0, gelu_mode);
+              z1 = gelu_f(z1, gelu_mode);
+            }
+            a[i] = __float_as_uint(z0);
+            a[i + 1] = __float_as_uint(z1);
+          }
         }
       }
       // 32 values = 4 x 16 bytes; 16-byte chunk j of this row goes to slot j ^ (row & 7)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int j = h * 4 + q;
-        const uint32_t addr = smem_u32(sbuf) + static_cast<uint32_t>(lane * 128) +
+        const uint32_t addr = smem_u32(stg) + static_cast<uint32_t>(lane * 128) +
                               static_cast<uint32_t>(((j ^ (lane & 7)) << 4));
-        const uint32_t p0 = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-        const uint32_t p1 = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-        const uint32_t p2 = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-        const uint32_t p3 = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p0),
-                     "r"(p1), "r"(p2), "r"(p3)
+        const uint32_t p0 = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
+        const uint32_t p1 = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
+        const uint32_t p2 = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
+        const uint32_t p3 = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p0), "r"(p1),
+                     "r"(p2), "r"(p3)
                      : "memory");
       }
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (row0 < M && n_chunk < N_out) tma_store_2d(tmY, sbuf, n_chunk, row0);
+      if (row0 < M && n_chunk < N_out) tma_store_2d(tmY, stg, n_chunk, row0);
       bulk_commit_group();
     }
-    sb ^= 1;
+    sb = (sb + 1) % kStgPerWarp;
   }
 }
 

@@ -36,8 +36,7 @@ namespace fmlp {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                 // 64 bf16 = 128 bytes = one swizzle row
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);   // producer, MMA issuer, epilogue warps
 constexpr int kRasterGroup = 16;        // M tiles per raster group (L2 reuse of weights)
 
 template <int BN, int EPI>
@@ -50,7 +49,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES =
-      1024 + STAGES * STAGE_BYTES + kEpiWarps * 2 * kStgBytes + BAR_BYTES;
+      1024 + STAGES * STAGE_BYTES + kEpiWarps * kStgPerWarp * kStgBytes + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256, "MMA N");
   static_assert(EPI != EPI_GEGLU || BN >= 128, "GeGLU needs 64-column output chunks");
   static_assert(BN_OUT % 64 == 0, "output chunks are 64 columns");
@@ -81,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   uint8_t* stg_all = smem + STAGES * C::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(stg_all + kEpiWarps * 2 * kStgBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_all + kEpiWarps * kStgPerWarp * kStgBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
-    uint8_t* stg = stg_all + (warp - 2) * 2 * kStgBytes;
+    uint8_t* stg = stg_all + (warp - 2) * kStgPerWarp * kStgBytes;
     int sb = 0;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -226,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
       const int row0 = tm * kBM + wq * 32;
-      epilogue_rows<BN, C::BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * C::BN_OUT, M, N_out,
+      epilogue_cols<BN, C::BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * C::BN_OUT, M, N_out,
                                         &tmY, bias, gelu_mode);
       // this warp is done reading the accumulator buffer
       tc_fence_before();

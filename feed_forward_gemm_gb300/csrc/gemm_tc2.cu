@@ -30,15 +30,15 @@ namespace {
 
 constexpr int kPairBN = 256;             // MMA N (both CTAs together)
 constexpr int kPairBK = 64;
-constexpr int kPairThreads = 192;
-constexpr int kPairEpiWarps = 4;
+constexpr int kPairThreads = 32 * (2 + kEpiWarps);
 constexpr int kPairGroup = 8;            // pair M tiles (256 rows) per raster group
 constexpr int kPairA = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kPairB = 128 * 128;        // this CTA's 128 B rows x 64 bf16
 constexpr int kPairStage = kPairA + kPairB;
 constexpr int kPairStages = 6;
 constexpr int kPairBar = (2 * kPairStages + 5) * 8 + 16;
-constexpr int kPairSmem = 1024 + kPairStages * kPairStage + kPairEpiWarps * 2 * kStgBytes + kPairBar;
+constexpr int kPairSmem =
+    1024 + kPairStages * kPairStage + kEpiWarps * kStgPerWarp * kStgBytes + kPairBar;
 static_assert(kPairSmem <= 232448, "shared memory");
 
 __device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, int& tm, int& tn) {
@@ -66,7 +66,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   uint8_t* stg_all = smem + kPairStages * kPairStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(stg_all + kPairEpiWarps * 2 * kStgBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_all + kEpiWarps * kStgPerWarp * kStgBytes);
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
   uint64_t* tempty = tfull + 2;
@@ -90,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * kPairEpiWarps * 32);
+      mbar_init(&tempty[b], 2 * kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
@@ -202,7 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int wq = warp & 3;
-    uint8_t* stg = stg_all + (warp - 2) * 2 * kStgBytes;
+    uint8_t* stg = stg_all + (warp - 2) * kStgPerWarp * kStgBytes;
     const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
     int sb = 0;
     int it = 0;
@@ -217,7 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
                              static_cast<uint32_t>(buf * kPairBN);
       const int row0 = tm * 256 + static_cast<int>(rank) * 128 + wq * 32;
-      epilogue_rows<kPairBN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
+      epilogue_cols<kPairBN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
                                           &tmY, bias, gelu_mode);
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf * 8));

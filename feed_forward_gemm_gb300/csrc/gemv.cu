@@ -3,54 +3,57 @@
 // At one token the feed-forward block reads every weight once and does one multiply-add per
 // weight, so it is bound by HBM bandwidth and by launch latency (ainews.cool fused-MLP
 // article, technical deep-dive: batch-1 decode pays one launch per layer and is limited by
-// memory traffic). The kernel is built for that:
-//   - each CTA owns a contiguous block of weight rows [r0, r1) (balanced to +-1 row), so the
-//     bytes it streams form one contiguous range per weight matrix;
-//   - one producer warp streams that range through a ring of 16 KB shared-memory slots with
-//     1-D bulk async copies (cp.async.bulk, completion counted on an mbarrier), keeping up to
-//     eight slots - 128 KB per SM - in flight; no register file is spent on loads in flight;
-//   - a slot is 32 segments of 512 bytes (one 16-byte vector per lane, 256 weights of one
-//     row); eight compute warps take four segments each, form the dot product with x (held
-//     in shared memory) in fp32, reduce it with warp shuffles and store one partial per
-//     (row, segment); one thread per (row, token) then adds a row's partials in segment
-//     order (deterministic) and applies the epilogue;
-//   - with two weight matrices (GeGLU gate and up) both ranges are streamed and the epilogue
+// memory traffic). The kernel is built to keep HBM busy:
+//   - each CTA owns a contiguous block of weight rows [r0, r1) (balanced to +-1 row), one CTA
+//     of 16 warps per SM, leaving the other half of the SM to the next layer's CTA;
+//   - the CTA's rows are cut into 512-byte segments (256 weights, one 16-byte vector per
+//     lane) and each warp takes one contiguous run of segments, so every warp streams its own
+//     contiguous range of W;
+//   - each lane streams its 16-byte pieces with asynchronous global->shared copies
+//     (cp.async, L2 only) through a private 3-stage ring of 4 segments per stage, so 12
+//     segments (6 KB) per warp and 96 KB per CTA are in flight without holding registers;
+//   - x (T x K bf16) sits in shared memory; each lane accumulates its dot products in fp32
+//     across the consecutive segments of one row and the warp reduces with shuffles only when
+//     its run crosses a row boundary. The reduced sum of a run piece is stored as the partial
+//     of the piece's first segment (the piece's other segments get 0), and one thread per
+//     (row, token) adds a row's partials in segment order: deterministic for a given shape;
+//   - with two weight matrices (GeGLU gate and up) both blocks are streamed and the epilogue
 //     forms gelu_tanh(g) * u;
 //   - programmatic dependent launch: the kernel lets the next kernel launch at once and
-//     prefetches its whole weight range into L2 before waiting for the previous kernel, so a
-//     layer's weights stream in while the previous layer finishes.
-// Every wait is bounded.
+//     prefetches its weight rows into L2 before waiting for the previous kernel, so a layer's
+//     weights start streaming while the previous layer finishes.
 #include "activation.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fmlp {
 
-constexpr int kGemvComputeWarps = 8;
-constexpr int kGemvThreads = (kGemvComputeWarps + 1) * 32;  // + one producer warp
-constexpr int kSeg = 256;                                    // weights per segment
-constexpr int kSegBytes = kSeg * 2;
-constexpr int kSlotSegs = 32;
-constexpr int kSlotBytes = kSlotSegs * kSegBytes;            // 16 KB
-constexpr int kMaxSlots = 8;
-constexpr int kMinSlots = 2;
+constexpr int kGemvThreads = 512;
+constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int kSeg = 256;                  // weights per segment (512 bytes)
+constexpr int kGemvCtasPerSm = 2;        // designed to leave room for a second resident CTA
+constexpr int kStageSegs = 4;              // segments per ring stage
+constexpr int kStages = 3;                 // ring stages per warp
+constexpr int kRingBytesPerWarp = kStages * kStageSegs * 512;
+constexpr int kRingBytes = kGemvWarps * kRingBytesPerWarp;   // 96 KB
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// 1-D bulk copy global -> this CTA's shared memory, completion counted on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ float dot8(uint4 w, uint4 x) {
-  float s = bf16_lo(w.x) * bf16_lo(x.x);
+__device__ __forceinline__ float dot8(uint4 w, uint4 x, float s) {
+  s = fmaf(bf16_lo(w.x), bf16_lo(x.x), s);
   s = fmaf(bf16_hi(w.x), bf16_hi(x.x), s);
   s = fmaf(bf16_lo(w.y), bf16_lo(x.y), s);
   s = fmaf(bf16_hi(w.y), bf16_hi(x.y), s);
@@ -61,66 +64,47 @@ __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
   return s;
 }
 
-struct GemvSmem {
-  size_t x_off, part_off, ring_off, bar_off, total;
-  int slots;
-};
-
-__host__ __device__ inline GemvSmem gemv_layout(int T, int K, int rows_max, int nmat,
-                                                size_t budget) {
-  GemvSmem L;
-  L.x_off = 0;
-  const size_t xb = static_cast<size_t>(T) * K * 2;
-  L.part_off = (xb + 15) & ~size_t(15);
-  const size_t pb = static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
-  L.ring_off = (L.part_off + pb + 1023) & ~size_t(1023);
-  const size_t fixed = L.ring_off + 2 * kMaxSlots * 8 + 1024;
-  int slots = kMinSlots;
-  if (budget > fixed) {
-    const size_t s = (budget - fixed) / kSlotBytes;
-    slots = s > kMaxSlots ? kMaxSlots : (s < kMinSlots ? kMinSlots : static_cast<int>(s));
+// Reduce a warp's per-lane sums (one per token), store them at part[pi .. pi+T), and clear
+// the accumulators.
+template <int TMAX>
+__device__ __forceinline__ void flush_piece(float (&acc)[TMAX], float* part, size_t pi, int T,
+                                            int lane) {
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
   }
-  L.slots = slots;
-  L.bar_off = L.ring_off + static_cast<size_t>(slots) * kSlotBytes;
-  L.total = L.bar_off + 2 * kMaxSlots * 8 + 1024;  // + alignment slack for the base
-  return L;
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+      if (t < T) part[pi + t] = acc[t];
+  }
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
 }
 
 template <int EPI, int NMAT, int TMAX>
-__global__ void __launch_bounds__(kGemvThreads, 1)
+__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
                 const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode,
-                int rows_max, int slots, int* status, uint64_t timeout_ns) {
-  extern __shared__ uint8_t gsm_raw[];
-  uint8_t* gsm = gsm_raw + ((1024u - (smem_u32(gsm_raw) & 1023u)) & 1023u);
-  const GemvSmem Ly = gemv_layout(T, K, rows_max, NMAT, 0);  // offsets only (slots from host)
+                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode) {
+  extern __shared__ __align__(16) uint8_t gsm[];
   const int r0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * N) / gridDim.x);
   const int r1 = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * N) / gridDim.x);
   const int rows = r1 - r0;
   const int segs = K / kSeg;
-  const int per_mat = rows * segs;                                   // segments per matrix
-  const int chunks_per_mat = (per_mat + kSlotSegs - 1) / kSlotSegs;
-  const int nchunks = NMAT * chunks_per_mat;
+  const int per_mat = rows * segs;
+  const int total = NMAT * per_mat;          // segments this CTA streams
 
-  uint4* xs = reinterpret_cast<uint4*>(gsm + Ly.x_off);              // [T][K/8]
-  float* part = reinterpret_cast<float*>(gsm + Ly.part_off);         // [mat][row][seg][T]
-  uint8_t* ring = gsm + Ly.ring_off;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(slots) * kSlotBytes);
-  uint64_t* empty = full + kMaxSlots;
+  uint8_t* ring = gsm;                                                    // [warp][stage][seg][lane]
+  uint4* xs = reinterpret_cast<uint4*>(gsm + kRingBytes);                 // [T][K/8]
+  float* part =
+      reinterpret_cast<float*>(gsm + kRingBytes + static_cast<size_t>(T) * K * 2);  // [seg][T]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < slots; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGemvComputeWarps);
-    }
-    fence_mbarrier_init();
-    pdl_launch_dependents();
-  }
+  if (threadIdx.x == 0) pdl_launch_dependents();
   // Warm L2 with this CTA's weight rows; they are not produced by the previous kernel.
-  if (warp == kGemvComputeWarps && lane < NMAT) {
-    const __nv_bfloat16* Wm = lane == 0 ? W0 : W1;
+  if (threadIdx.x < NMAT) {
+    const __nv_bfloat16* Wm = threadIdx.x == 0 ? W0 : W1;
     const char* base = reinterpret_cast<const char*>(Wm + static_cast<size_t>(r0) * K);
     const size_t bytes = static_cast<size_t>(rows) * K * 2;
     for (size_t off = 0; off < bytes; off += 65536) {
@@ -128,80 +112,78 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       prefetch_l2_bulk(base + off, static_cast<uint32_t>(n));
     }
   }
-  __syncthreads();
   pdl_wait_primary();
 
-  if (warp == kGemvComputeWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t issued = 0, last_par = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % slots;
-        const uint32_t par = static_cast<uint32_t>(c / slots) & 1u;
-        if (!mbar_wait(&empty[s], par ^ 1u, status, SITE_GEMV, timeout_ns)) break;
-        const int mat = NMAT == 2 ? c / chunks_per_mat : 0;
-        const int cm = c - mat * chunks_per_mat;
-        const int seg0 = cm * kSlotSegs;
-        const int nseg = per_mat - seg0 < kSlotSegs ? per_mat - seg0 : kSlotSegs;
+  const int xvec = T * (K / 8);
+  for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
+    xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+  __syncthreads();
+
+  // warp w streams segments [g0, g1) of the CTA's list (matrix-major, then row, then segment)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g0 = static_cast<int>((static_cast<int64_t>(warp) * total) / kGemvWarps);
+  const int g1 = static_cast<int>((static_cast<int64_t>(warp + 1) * total) / kGemvWarps);
+  float acc[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
+  size_t piece_pi = 0;  // its partial index
+  // this lane's slice of the warp's ring: stage s, segment j at + (s * kStageSegs + j) * 512
+  const uint32_t my_ring = smem_u32(ring) + static_cast<uint32_t>(warp * kRingBytesPerWarp +
+                                                                  lane * 16);
+  auto issue_stage = [&](int stage_no) {
+    const int slot = stage_no % kStages;
+#pragma unroll
+    for (int j = 0; j < kStageSegs; ++j) {
+      const int g = g0 + stage_no * kStageSegs + j;
+      if (g < g1) {
+        const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
+        const int gm = g - mat * per_mat;
         const __nv_bfloat16* Wm = mat ? W1 : W0;
-        const char* src = reinterpret_cast<const char*>(Wm + static_cast<size_t>(r0) * K) +
-                          static_cast<size_t>(seg0) * kSegBytes;
-        const uint32_t bytes = static_cast<uint32_t>(nseg) * kSegBytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_load(ring + static_cast<size_t>(s) * kSlotBytes, src, bytes, &full[s]);
-        issued |= 1u << s;
-        last_par = (last_par & ~(1u << s)) | (par << s);
+        // consecutive segments of a matrix block are consecutive 512-byte pieces of memory
+        cp_async_16(my_ring + static_cast<uint32_t>((slot * kStageSegs + j) * 512),
+                    Wm + static_cast<size_t>(r0) * K + static_cast<size_t>(gm) * kSeg + lane * 8);
       }
-      // every copy issued must land before the CTA can exit (normally consumed already)
-      for (int s = 0; s < slots; ++s)
-        if (issued & (1u << s))
-          mbar_wait(&full[s], (last_par >> s) & 1u, status, SITE_DRAIN, timeout_ns);
     }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ compute warps
-    const int xvec = T * (K / 8);
-    for (int i = threadIdx.x; i < xvec; i += kGemvComputeWarps * 32)
-      xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
-    asm volatile("bar.sync 1, %0;" ::"n"(kGemvComputeWarps * 32) : "memory");
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c % slots;
-      const uint32_t par = static_cast<uint32_t>(c / slots) & 1u;
-      const bool ok = mbar_wait(&full[s], par, status, SITE_GEMV, timeout_ns);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const int mat = NMAT == 2 ? c / chunks_per_mat : 0;
-      const int cm = c - mat * chunks_per_mat;
-      const int seg0 = cm * kSlotSegs;
-      const uint8_t* slot = ring + static_cast<size_t>(s) * kSlotBytes;
+    cp_async_commit();   // one group per stage (possibly empty), so the wait counts line up
+  };
+  const int nstage = (g1 - g0 + kStageSegs - 1) / kStageSegs;
 #pragma unroll
-      for (int j = warp; j < kSlotSegs; j += kGemvComputeWarps) {
-        const int g = seg0 + j;   // segment index within this matrix block
-        if (g < per_mat) {        // warp-uniform
-          const int row = g / segs, seg = g - row * segs;
-          const uint4 wv = *reinterpret_cast<const uint4*>(slot + j * kSegBytes + lane * 16);
-          float p[TMAX];
+  for (int p = 0; p < kStages; ++p) issue_stage(p);
+  for (int st = 0; st < nstage; ++st) {
+    cp_async_wait<kStages - 1>();   // this lane's copies of stage st have landed
+    const int slot = st % kStages;
 #pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            p[t] = 0.f;
-            if (t < T) p[t] = dot8(wv, xs[t * (K / 8) + seg * (kSeg / 8) + lane]);
-          }
+    for (int j = 0; j < kStageSegs; ++j) {
+      const int g = g0 + st * kStageSegs + j;
+      if (g >= g1) break;  // warp-uniform
+      const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
+      const int gm = g - mat * per_mat;
+      const int row = gm / segs, seg = gm - row * segs;
+      const int rid = mat * rows + row;
+      const size_t pi = static_cast<size_t>(g) * T;
+      if (rid != piece_row) {
+        if (piece_row >= 0) flush_piece<TMAX>(acc, part, piece_pi, T, lane);
+        piece_row = rid;
+        piece_pi = pi;
+      } else if (lane == 0) {
 #pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) p[t] += __shfl_xor_sync(0xffffffffu, p[t], o);
-          }
-          if (lane == 0) {
-            const size_t pi = (static_cast<size_t>(mat) * per_mat + row * segs + seg) * T;
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t)
-              if (t < T) part[pi + t] = p[t];
-          }
-        }
+        for (int t = 0; t < TMAX; ++t)
+          if (t < T) part[pi + t] = 0.f;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      uint4 wv;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w)
+                   : "r"(my_ring + static_cast<uint32_t>((slot * kStageSegs + j) * 512)));
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t)
+        if (t < T) acc[t] = dot8(wv, xs[t * (K / 8) + seg * (kSeg / 8) + lane], acc[t]);
     }
+    // the lane has read this slot (its own bytes); refill it with stage st + kStages
+    issue_stage(st + kStages);
   }
+  cp_async_wait<0>();
+  if (piece_row >= 0) flush_piece<TMAX>(acc, part, piece_pi, T, lane);
   __syncthreads();
 
   // one thread per (row, token): add the segments in order, then the epilogue
@@ -225,21 +207,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
-  const int rows_max = static_cast<int>((static_cast<int64_t>(N) + grid - 1) / grid);
-  return gemv_layout(T, K, rows_max, nmat, kGemvPreferSmem).total;
+  const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
+  return kRingBytes + static_cast<size_t>(T) * K * 2 +
+         static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+}
+
+// One CTA per SM: each CTA uses at most half of an SM's threads, registers and (for most
+// shapes) shared memory, so the next kernel's CTAs - the next layer, launched early as a
+// programmatic dependent - can sit beside it and prefetch their weights while this one runs.
+int gemv_grid(int T, int K, int N, int nmat, int sms) {
+  (void)T;
+  (void)K;
+  (void)nmat;
+  return sms < N ? sms : N;
 }
 
 template <int EPI, int NMAT, int TMAX>
-static cudaError_t gemv_launch_t(const GemvLaunch& L, const GemvSmem& lay, int rows_max) {
+static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
   auto kern = gemv_kernel<EPI, NMAT, TMAX>;
   static SmemAttrCache cache;
   cudaError_t e =
-      set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(lay.total), cache);
+      set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem), cache);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
-  cfg.dynamicSmemBytes = lay.total;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -250,27 +243,25 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, const GemvSmem& lay, int r
                             static_cast<const __nv_bfloat16*>(L.W0),
                             static_cast<const __nv_bfloat16*>(L.W1),
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode,
-                            rows_max, lay.slots, L.status, L.timeout_ns);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode);
 }
 
 cudaError_t gemv_launch(const GemvLaunch& L) {
   const int nmat = L.epi == EPI_GEGLU ? 2 : 1;
-  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || L.grid < 1) return cudaErrorInvalidValue;
-  const int rows_max = static_cast<int>((static_cast<int64_t>(L.N) + L.grid - 1) / L.grid);
-  const GemvSmem lay = gemv_layout(L.T, L.K, rows_max, nmat, kGemvPreferSmem);
-  if (lay.total > kGemvMaxSmem) return cudaErrorInvalidValue;
+  const size_t smem = gemv_smem_bytes(L.T, L.K, L.N, nmat, L.grid);
+  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || L.grid < 1 || smem > kGemvMaxSmem)
+    return cudaErrorInvalidValue;
   if (L.T == 1) {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1>(L, lay, rows_max);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1>(L, lay, rows_max);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1>(L, lay, rows_max);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1>(L, smem);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1>(L, smem);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1>(L, smem);
     }
   } else {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT>(L, lay, rows_max);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT>(L, lay, rows_max);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT>(L, lay, rows_max);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT>(L, smem);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT>(L, smem);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT>(L, smem);
     }
   }
   return cudaErrorInvalidValue;

@@ -68,10 +68,7 @@ int gemm_tc_smem_bytes(int epi, int bn);
 
 // Weight-streaming GEMV for T <= kGemvMaxT tokens (decode).
 constexpr int kGemvMaxT = 4;
-// Shared memory: the ring of weight slots is sized to fit kGemvPreferSmem (two CTAs per SM, so
-// the next layer's CTAs can start while this layer runs); shapes whose x and partial sums need
-// more may use up to kGemvMaxSmem with the minimum ring.
-constexpr size_t kGemvPreferSmem = 112 * 1024;
+// Shared memory holds x and the per-segment partial sums.
 constexpr size_t kGemvMaxSmem = 200 * 1024;
 struct GemvLaunch {
   const void* x;      // [T, K]
@@ -84,9 +81,9 @@ struct GemvLaunch {
   int gelu_mode;
   int grid;
   cudaStream_t stream;
-  int* status;
-  uint64_t timeout_ns;
 };
+// CTAs of the GEMV (nmat weight matrices of [N, K], T tokens) on a device with `sms` SMs.
+int gemv_grid(int T, int K, int N, int nmat, int sms);
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);
 cudaError_t gemv_launch(const GemvLaunch& L);
 

@@ -31,7 +31,6 @@ namespace {
 constexpr int kPairBN = 256;             // MMA N (both CTAs together)
 constexpr int kPairBK = 64;
 constexpr int kPairThreads = 32 * (2 + kEpiWarps);
-constexpr int kPairGroup = 8;            // pair M tiles (256 rows) per raster group
 constexpr int kPairA = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kPairB = 128 * 128;        // this CTA's 128 B rows x 64 bf16
 constexpr int kPairStage = kPairA + kPairB;
@@ -41,11 +40,14 @@ constexpr int kPairSmem =
     1024 + kPairStages * kPairStage + kEpiWarps * kStgPerWarp * kStgBytes + kPairBar;
 static_assert(kPairSmem <= 232448, "shared memory");
 
-__device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, int& tm, int& tn) {
-  const int per_group = kPairGroup * num_n;
+// Tiles are walked in groups of `group` M tiles (256 rows each) across all N tiles, M fastest,
+// so the pairs in flight share a band of x rows and a few weight panels in L2.
+__device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, int group, int& tm,
+                                                 int& tn) {
+  const int per_group = group * num_n;
   const int g = t / per_group;
-  const int first_m = g * kPairGroup;
-  const int gm = min(num_m - first_m, kPairGroup);
+  const int first_m = g * group;
+  const int gm = min(num_m - first_m, group);
   const int r = t - g * per_group;
   tm = first_m + r % gm;
   tn = r / gm;
@@ -60,7 +62,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmY,
                     const __nv_bfloat16* __restrict__ bias, int M, int N_out, int K,
-                    int gelu_mode, int* status, uint64_t timeout_ns) {
+                    int gelu_mode, int group, int* status, uint64_t timeout_ns) {
   constexpr int BN_OUT = EPI == EPI_GEGLU ? kPairBN / 2 : kPairBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -123,7 +125,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         int tm, tn;
-        pair_tile_coords(t, num_m, num_n, tm, tn);
+        pair_tile_coords(t, num_m, num_n, group, tm, tn);
         const int a_row = tm * 256 + static_cast<int>(rank) * 128;
         const CUtensorMap* bmap = &tmB0;
         int b_row;
@@ -208,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int it = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++it) {
       int tm, tn;
-      pair_tile_coords(t, num_m, num_n, tm, tn);
+      pair_tile_coords(t, num_m, num_n, group, tm, tn);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       const bool ok = mbar_wait(&tfull[buf], use, status, SITE_EPI_TMEM_FULL, timeout_ns);
@@ -253,9 +255,13 @@ static cudaError_t launch_pair(const GemmLaunch& L) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.pdl ? 1 : 0;
+  // Raster group: as many 256-row bands of A as fit in about 64 MB of L2 (at least 2, at most
+  // 16; 16 measured best for the 8192-wide, K = 8192 gate/up GEMM).
+  int group = static_cast<int>((64ll << 20) / (256ll * L.K * 2));
+  group = group < 2 ? 2 : (group > 16 ? 16 : group);
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB0, L.tmB1, L.tmY,
                             static_cast<const __nv_bfloat16*>(L.bias), L.M, L.N_out, L.K,
-                            L.gelu_mode, L.status, L.timeout_ns);
+                            L.gelu_mode, group, L.status, L.timeout_ns);
 }
 
 cudaError_t gemm_tc2_launch(const GemmLaunch& L) {

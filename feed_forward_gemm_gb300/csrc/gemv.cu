@@ -4,24 +4,25 @@
 // weight, so it is bound by HBM bandwidth and by launch latency (ainews.cool fused-MLP
 // article, technical deep-dive: batch-1 decode pays one launch per layer and is limited by
 // memory traffic). The kernel is built to keep HBM busy:
-//   - each CTA owns a contiguous block of weight rows [r0, r1) (balanced to +-1 row), one CTA
-//     of 16 warps per SM, leaving the other half of the SM to the next layer's CTA;
+//   - each CTA owns a contiguous block of weight rows [r0, r1) (balanced to +-1 row), two
+//     CTAs of 16 warps per SM;
 //   - the CTA's rows are cut into 512-byte segments (256 weights, one 16-byte vector per
 //     lane) and each warp takes one contiguous run of segments, so every warp streams its own
-//     contiguous range of W;
-//   - each lane streams its 16-byte pieces with asynchronous global->shared copies
-//     (cp.async, L2 only) through a private 3-stage ring of 4 segments per stage, so 12
-//     segments (6 KB) per warp and 96 KB per CTA are in flight without holding registers;
+//     contiguous range of W with 8 non-allocating 128-bit loads per lane in flight;
+//   - programmatic dependent launch: the kernel lets the next kernel launch at once and
+//     prefetches its weight rows into L2 before waiting for the previous kernel; after the
+//     wait, the first batch of weight loads is issued before x is staged, so the x load hides
+//     under them;
+//   - when the caller names the next layer's weights (the second GEMV of the same block) and
+//     they fit in L2, each CTA also prefetches its share of them into L2, so the second layer
+//     streams them from L2 while HBM serves both layers back to back;
 //   - x (T x K bf16) sits in shared memory; each lane accumulates its dot products in fp32
 //     across the consecutive segments of one row and the warp reduces with shuffles only when
 //     its run crosses a row boundary. The reduced sum of a run piece is stored as the partial
 //     of the piece's first segment (the piece's other segments get 0), and one thread per
 //     (row, token) adds a row's partials in segment order: deterministic for a given shape;
 //   - with two weight matrices (GeGLU gate and up) both blocks are streamed and the epilogue
-//     forms gelu_tanh(g) * u;
-//   - programmatic dependent launch: the kernel lets the next kernel launch at once and
-//     prefetches its weight rows into L2 before waiting for the previous kernel, so a layer's
-//     weights start streaming while the previous layer finishes.
+//     forms gelu_tanh(g) * u.
 #include "activation.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -31,21 +32,15 @@ namespace fmlp {
 constexpr int kGemvThreads = 512;
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kSeg = 256;                  // weights per segment (512 bytes)
-constexpr int kGemvCtasPerSm = 2;        // designed to leave room for a second resident CTA
-constexpr int kStageSegs = 4;              // segments per ring stage
-constexpr int kStages = 3;                 // ring stages per warp
-constexpr int kRingBytesPerWarp = kStages * kStageSegs * 512;
-constexpr int kRingBytes = kGemvWarps * kRingBytesPerWarp;   // 96 KB
+constexpr int kGemvCtasPerSm = 2;
+constexpr int kGemvBatch = 8;              // 16-byte loads in flight per lane
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
@@ -83,79 +78,80 @@ __device__ __forceinline__ void flush_piece(float (&acc)[TMAX], float* part, siz
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
 }
 
-template <int EPI, int NMAT, int TMAX>
-__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
-    gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
-                const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode) {
-  extern __shared__ __align__(16) uint8_t gsm[];
-  const int r0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * N) / gridDim.x);
-  const int r1 = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * N) / gridDim.x);
+// L2 prefetch of rows [r0, r1) of a [*, K] bf16 matrix.
+__device__ __forceinline__ void prefetch_rows(const __nv_bfloat16* W, int r0, int r1, int K) {
+  const char* base = reinterpret_cast<const char*>(W + static_cast<size_t>(r0) * K);
+  const size_t bytes = static_cast<size_t>(r1 - r0) * K * 2;
+  for (size_t off = 0; off < bytes; off += 65536) {
+    const size_t n = bytes - off < 65536 ? bytes - off : 65536;
+    prefetch_l2_bulk(base + off, static_cast<uint32_t>(n));
+  }
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// One layer for this CTA's rows [r0, r1) of W (NMAT matrices): y[t, n] for n in [r0, r1).
+// All threads of the CTA take part (it synchronises internally). X_COHERENT reads x through
+// L2 instead of the read-only path (for x written by other CTAs of the same kernel).
+template <int EPI, int NMAT, int TMAX, bool X_COHERENT>
+__device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __restrict__ x,
+                                          const __nv_bfloat16* __restrict__ W0,
+                                          const __nv_bfloat16* __restrict__ W1,
+                                          const __nv_bfloat16* __restrict__ bias,
+                                          __nv_bfloat16* __restrict__ y, int T, int K, int N,
+                                          int gelu_mode, int r0, int r1) {
   const int rows = r1 - r0;
   const int segs = K / kSeg;
   const int per_mat = rows * segs;
   const int total = NMAT * per_mat;          // segments this CTA streams
-
-  uint8_t* ring = gsm;                                                    // [warp][stage][seg][lane]
-  uint4* xs = reinterpret_cast<uint4*>(gsm + kRingBytes);                 // [T][K/8]
-  float* part =
-      reinterpret_cast<float*>(gsm + kRingBytes + static_cast<size_t>(T) * K * 2);  // [seg][T]
-
-  if (threadIdx.x == 0) pdl_launch_dependents();
-  // Warm L2 with this CTA's weight rows; they are not produced by the previous kernel.
-  if (threadIdx.x < NMAT) {
-    const __nv_bfloat16* Wm = threadIdx.x == 0 ? W0 : W1;
-    const char* base = reinterpret_cast<const char*>(Wm + static_cast<size_t>(r0) * K);
-    const size_t bytes = static_cast<size_t>(rows) * K * 2;
-    for (size_t off = 0; off < bytes; off += 65536) {
-      const size_t n = bytes - off < 65536 ? bytes - off : 65536;
-      prefetch_l2_bulk(base + off, static_cast<uint32_t>(n));
-    }
-  }
-  pdl_wait_primary();
-
-  const int xvec = T * (K / 8);
-  for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
-    xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
-  __syncthreads();
+  uint4* xs = reinterpret_cast<uint4*>(gsm);                                     // [T][K/8]
+  float* part = reinterpret_cast<float*>(gsm + static_cast<size_t>(T) * K * 2);  // [seg][T]
 
   // warp w streams segments [g0, g1) of the CTA's list (matrix-major, then row, then segment)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g0 = static_cast<int>((static_cast<int64_t>(warp) * total) / kGemvWarps);
   const int g1 = static_cast<int>((static_cast<int64_t>(warp + 1) * total) / kGemvWarps);
-  float acc[TMAX];
+  uint4 wv[kGemvBatch];
+  auto load_batch = [&](int base) {
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-  int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
-  size_t piece_pi = 0;  // its partial index
-  // this lane's slice of the warp's ring: stage s, segment j at + (s * kStageSegs + j) * 512
-  const uint32_t my_ring = smem_u32(ring) + static_cast<uint32_t>(warp * kRingBytesPerWarp +
-                                                                  lane * 16);
-  auto issue_stage = [&](int stage_no) {
-    const int slot = stage_no % kStages;
-#pragma unroll
-    for (int j = 0; j < kStageSegs; ++j) {
-      const int g = g0 + stage_no * kStageSegs + j;
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int g = base + u;
       if (g < g1) {
         const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
         const int gm = g - mat * per_mat;
         const __nv_bfloat16* Wm = mat ? W1 : W0;
         // consecutive segments of a matrix block are consecutive 512-byte pieces of memory
-        cp_async_16(my_ring + static_cast<uint32_t>((slot * kStageSegs + j) * 512),
-                    Wm + static_cast<size_t>(r0) * K + static_cast<size_t>(gm) * kSeg + lane * 8);
+        wv[u] = ld_stream_v4(Wm + static_cast<size_t>(r0) * K + static_cast<size_t>(gm) * kSeg +
+                             lane * 8);
+      } else {
+        wv[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    cp_async_commit();   // one group per stage (possibly empty), so the wait counts line up
   };
-  const int nstage = (g1 - g0 + kStageSegs - 1) / kStageSegs;
+  load_batch(g0);   // in flight while x is staged
+
+  const int xvec = T * (K / 8);
+  for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
+    xs[i] = X_COHERENT ? ld_cg_v4(reinterpret_cast<const uint4*>(x) + i)
+                       : __ldg(reinterpret_cast<const uint4*>(x) + i);
+  __syncthreads();
+
+  float acc[TMAX];
 #pragma unroll
-  for (int p = 0; p < kStages; ++p) issue_stage(p);
-  for (int st = 0; st < nstage; ++st) {
-    cp_async_wait<kStages - 1>();   // this lane's copies of stage st have landed
-    const int slot = st % kStages;
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
+  size_t piece_pi = 0;  // its partial index
+  for (int base = g0; base < g1; base += kGemvBatch) {
+    if (base != g0) load_batch(base);
 #pragma unroll
-    for (int j = 0; j < kStageSegs; ++j) {
-      const int g = g0 + st * kStageSegs + j;
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int g = base + u;
       if (g >= g1) break;  // warp-uniform
       const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
       const int gm = g - mat * per_mat;
@@ -171,18 +167,11 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
         for (int t = 0; t < TMAX; ++t)
           if (t < T) part[pi + t] = 0.f;
       }
-      uint4 wv;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w)
-                   : "r"(my_ring + static_cast<uint32_t>((slot * kStageSegs + j) * 512)));
 #pragma unroll
       for (int t = 0; t < TMAX; ++t)
-        if (t < T) acc[t] = dot8(wv, xs[t * (K / 8) + seg * (kSeg / 8) + lane], acc[t]);
+        if (t < T) acc[t] = dot8(wv[u], xs[t * (K / 8) + seg * (kSeg / 8) + lane], acc[t]);
     }
-    // the lane has read this slot (its own bytes); refill it with stage st + kStages
-    issue_stage(st + kStages);
   }
-  cp_async_wait<0>();
   if (piece_row >= 0) flush_piece<TMAX>(acc, part, piece_pi, T, lane);
   __syncthreads();
 
@@ -204,22 +193,51 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     }
     y[static_cast<size_t>(t) * N + n] = __float2bfloat16_rn(v);
   }
+  __syncthreads();   // the shared memory may be reused by the caller
+}
+
+__device__ __forceinline__ int split_row(int i, int N) {
+  return static_cast<int>((static_cast<int64_t>(i) * N) / gridDim.x);
+}
+
+template <int EPI, int NMAT, int TMAX>
+__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
+    gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
+                const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
+                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode,
+                const char* __restrict__ next_w, size_t next_bytes) {
+  extern __shared__ __align__(16) uint8_t gsm[];
+  const int r0 = split_row(blockIdx.x, N), r1 = split_row(blockIdx.x + 1, N);
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  // Warm L2 with this CTA's weight rows; they are not produced by the previous kernel.
+  if (threadIdx.x == 0) prefetch_rows(W0, r0, r1, K);
+  if (NMAT == 2 && threadIdx.x == 1) prefetch_rows(W1, r0, r1, K);
+  // This CTA's 1/gridDim share of the next layer's weights (16-byte granules).
+  if (next_w != nullptr && threadIdx.x == 32) {
+    const size_t gran = next_bytes / 16;
+    const size_t b0 = (gran * blockIdx.x) / gridDim.x * 16, b1 = (gran * (blockIdx.x + 1)) / gridDim.x * 16;
+    for (size_t off = b0; off < b1; off += 65536) {
+      const size_t n = b1 - off < 65536 ? b1 - off : 65536;
+      prefetch_l2_bulk(next_w + off, static_cast<uint32_t>(n));
+    }
+  }
+  pdl_wait_primary();
+  gemv_rows<EPI, NMAT, TMAX, false>(gsm, x, W0, W1, bias, y, T, K, N, gelu_mode, r0, r1);
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
   const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
-  return kRingBytes + static_cast<size_t>(T) * K * 2 +
+  return static_cast<size_t>(T) * K * 2 +
          static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
 }
 
-// One CTA per SM: each CTA uses at most half of an SM's threads, registers and (for most
-// shapes) shared memory, so the next kernel's CTAs - the next layer, launched early as a
-// programmatic dependent - can sit beside it and prefetch their weights while this one runs.
+// Two CTAs per SM (each at most half of an SM's registers and threads).
 int gemv_grid(int T, int K, int N, int nmat, int sms) {
   (void)T;
   (void)K;
   (void)nmat;
-  return sms < N ? sms : N;
+  const int g = sms * kGemvCtasPerSm;
+  return g < N ? g : N;
 }
 
 template <int EPI, int NMAT, int TMAX>
@@ -243,7 +261,8 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
                             static_cast<const __nv_bfloat16*>(L.W0),
                             static_cast<const __nv_bfloat16*>(L.W1),
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode,
+                            static_cast<const char*>(L.next_w), L.next_bytes);
 }
 
 cudaError_t gemv_launch(const GemvLaunch& L) {

@@ -237,27 +237,60 @@ def run_ours(args, dist: Dist):
         raise SystemExit(f"device status after timing: {fm.fmlp_last_error()}")
 
     # ---------------- end to end through the C ABI with host buffers
+    # Every step copies its x from pinned host memory and its y back. Copies run on their own
+    # streams into double-buffered device tensors, so step i's copies overlap the compute of
+    # its neighbours, as a serving loop would run; each step's copies and compute are all
+    # inside the timed region.
     x_host = torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(x)
+    y_host = [torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_used = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):   # start with every buffer free
+        ev_used[b].record(stream)
+        ev_out[b].record(stream)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        fm.fmlp_geglu(x_dev, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, ws_bytes, stream)
-        y_host.copy_(y, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        h2d.wait_event(ev_used[b])            # step i-2's compute is done with x_dev[b]
+        with torch.cuda.stream(h2d):
+            x_dev[b].copy_(x_host, non_blocking=True)
+        ev_in[b].record(h2d)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])          # step i-2's result has left y_dev[b]
+        fm.fmlp_geglu(x_dev[b], Wg, Wu, Wd, y_dev[b], w.T, w.D, w.H, ws, ws_bytes, stream)
+        ev_used[b].record(stream)
+        d2h.wait_event(ev_used[b])
+        with torch.cuda.stream(d2h):
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+        ev_out[b].record(d2h)
 
-    for _ in range(2):
-        e2e_step()
-    e2e_iters = max(3, args.steps // 2)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e2e_iters = max(6, args.steps // 2)
     dist.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    e2e_ms = events_time(e2e_step, e2e_iters)
+    t_start.record(h2d)
+    for i in range(e2e_iters):
+        e2e_step(i)
+    stream.wait_stream(d2h)
+    t_end.record(stream)
+    t_end.synchronize()
     wall_ms = (time.perf_counter() - t0) * 1e3 / e2e_iters
-    e2e_ms = dist.max(max(e2e_ms, wall_ms), dev)
+    e2e_ms = max(t_start.elapsed_time(t_end) / e2e_iters, wall_ms)
+    e2e_ms = dist.max(e2e_ms, dev)
     e2e = {"value": round(dist.world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
-           "ms_per_step": round(e2e_ms, 4)}
-    del x_host, y_host, x_dev
+           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host[0].numel() * 2,
+           "ms_per_step": round(e2e_ms, 4),
+           "method": "pinned host x -> device, fmlp_geglu, y -> pinned host every step; copies on "
+                     "their own streams, double-buffered, overlapping neighbouring steps"}
+    del x_host, y_host, x_dev, y_dev
 
     extras = {}
     if not args.no_extras:

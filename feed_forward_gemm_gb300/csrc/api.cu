@@ -231,13 +231,13 @@ int pick_bn(int64_t M, int64_t N_out, int sms, bool geglu, double* cost_out) {
   return best;
 }
 
-// The CTA-pair kernel computes 256x256 tiles with two SMs; per SM that is the work of one
-// 128x256 single-SM tile with a third less operand traffic, hence its efficiency edge.
+// Per-clock efficiency of the CTA-pair kernel relative to the single-SM 128x256 tile, from ncu
+// durations on GB300 (it moves a third less operand data per SM).
 constexpr double kPairEff = 1.3;
 
 struct GemmChoice {
-  bool pair;   // CTA-pair kernel (256x256 tiles) instead of the single-SM kernel
-  int bn;      // MMA N of the single-SM kernel (256 for the pair kernel)
+  bool pair;   // CTA-pair kernel (256-row tiles) instead of the single-SM kernel
+  int bn;      // MMA N: 64/128/256 (single SM) or 256 (pair)
   int grid;    // CTAs launched
 };
 
@@ -245,22 +245,30 @@ GemmChoice choose_gemm(const DeviceState& d, int epi, int64_t M, int64_t N_out) 
   GemmChoice c;
   const bool geglu = epi == EPI_GEGLU;
   double cost1 = 0;
-  c.bn = pick_bn(M, N_out, d.sms, geglu, &cost1);
+  const int bn1 = pick_bn(M, N_out, d.sms, geglu, &cost1);
   c.pair = false;
+  c.bn = bn1;
   const int policy = g_tile_policy.load(std::memory_order_relaxed);
-  int pairs = 0;
+  double best = (policy == FMLP_TILES_AUTO || policy == FMLP_TILES_SINGLE) ? cost1 : 1e300;
+  int pairs_best = 0;
   if (d.max_pairs >= 1 && M > 128 && policy != FMLP_TILES_SINGLE) {
-    const int bn_out2 = geglu ? 128 : 256;
-    const int64_t tiles2 = ((M + 255) / 256) * ((N_out + bn_out2 - 1) / bn_out2);
-    pairs = static_cast<int>(std::min<int64_t>(tiles2, d.max_pairs));
+    const int bn = 256;
+    const int bn_out = geglu ? bn / 2 : bn;
+    const int64_t tiles2 = ((M + 255) / 256) * ((N_out + bn_out - 1) / bn_out);
+    const int pairs = static_cast<int>(std::min<int64_t>(tiles2, d.max_pairs));
     const int64_t waves2 = (tiles2 + pairs - 1) / pairs;
-    const double cost2 = static_cast<double>(waves2) * 256 / kPairEff;
-    c.pair = policy == FMLP_TILES_PAIR || cost2 < cost1;
+    const double cost = static_cast<double>(waves2) * bn / kPairEff;
+    if (cost < best || policy == FMLP_TILES_PAIR) {
+      best = cost;
+      c.pair = true;
+      c.bn = bn;
+      pairs_best = pairs;
+    }
   }
   if (c.pair) {
-    c.bn = 256;
-    c.grid = 2 * pairs;
+    c.grid = 2 * pairs_best;
   } else {
+    c.bn = bn1;
     const int bn_out = geglu ? c.bn / 2 : c.bn;
     const int64_t tiles = ((M + 127) / 128) * ((N_out + bn_out - 1) / bn_out);
     c.grid = static_cast<int>(std::min<int64_t>(tiles, d.sms));
@@ -277,7 +285,7 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   const GemmChoice ch = choose_gemm(d, epi, M, N_out);
   const bool pair = ch.pair;
   L.bn = ch.bn;
-  const uint32_t b_rows = pair ? 128u : (geglu ? L.bn / 2 : L.bn);
+  const uint32_t b_rows = static_cast<uint32_t>(pair || geglu ? L.bn / 2 : L.bn);
   FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A"));
   FMLP_TRY(make_map(&L.tmB0, B0, N_out, K, b_rows, "B"));
   if (geglu) {
@@ -625,8 +633,8 @@ static std::string describe_gemm(const DeviceState& d, const char* name, int epi
   const GemmChoice c = choose_gemm(d, epi, M, N);
   char b[256];
   if (c.pair)
-    snprintf(b, sizeof b, "%s: tcgen05 CTA-pair 256x256 tiles, M=%lld N=%lld K=%lld, grid=%d",
-             name, static_cast<long long>(M), static_cast<long long>(N),
+    snprintf(b, sizeof b, "%s: tcgen05 CTA-pair 256x%d tiles, M=%lld N=%lld K=%lld, grid=%d",
+             name, c.bn, static_cast<long long>(M), static_cast<long long>(N),
              static_cast<long long>(K), c.grid);
   else
     snprintf(b, sizeof b, "%s: tcgen05 single-SM 128x%d tiles, M=%lld N=%lld K=%lld, grid=%d",

@@ -28,17 +28,24 @@ namespace fmlp {
 
 namespace {
 
-constexpr int kPairBN = 256;             // MMA N (both CTAs together)
 constexpr int kPairBK = 64;
 constexpr int kPairThreads = 32 * (2 + kEpiWarps);
-constexpr int kPairA = 128 * 128;        // 128 rows x 64 bf16
-constexpr int kPairB = 128 * 128;        // this CTA's 128 B rows x 64 bf16
-constexpr int kPairStage = kPairA + kPairB;
-constexpr int kPairStages = 6;
-constexpr int kPairBar = (2 * kPairStages + 5) * 8 + 16;
-constexpr int kPairSmem =
-    1024 + kPairStages * kPairStage + kEpiWarps * kStgPerWarp * kStgBytes + kPairBar;
-static_assert(kPairSmem <= 232448, "shared memory");
+constexpr int kPairA = 128 * 128;        // this CTA's 128 A rows x 64 bf16
+
+// BN: MMA N of the pair (both CTAs' B rows together). Only 256 is instantiated: a 256x128
+// pair tile was measured 1.6-1.8x slower per unit of work on GB300.
+template <int BN>
+struct PairCfg {
+  static constexpr int B_BYTES = (BN / 2) * 128;   // this CTA's BN/2 B rows x 64 bf16
+  static constexpr int STAGE = kPairA + B_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE;
+  static constexpr int BAR = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + kEpiWarps * kStgPerWarp * kStgBytes + BAR;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(BN == 128 || BN == 256, "pair tile width");
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(B_BYTES % 1024 == 0, "1024-byte aligned B tiles");
+};
 
 // Tiles are walked in groups of `group` M tiles (256 rows each) across all N tiles, M fastest,
 // so the pairs in flight share a band of x rows and a few weight panels in L2.
@@ -55,7 +62,7 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, in
 
 }  // namespace
 
-template <int EPI>
+template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB0,
@@ -63,7 +70,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     const __grid_constant__ CUtensorMap tmY,
                     const __nv_bfloat16* __restrict__ bias, int M, int N_out, int K,
                     int gelu_mode, int group, int* status, uint64_t timeout_ns) {
-  constexpr int BN_OUT = EPI == EPI_GEGLU ? kPairBN / 2 : kPairBN;
+  using C = PairCfg<BN>;
+  constexpr int kPairStages = C::STAGES;
+  constexpr int kPairStage = C::STAGE;
+  constexpr int BN_OUT = EPI == EPI_GEGLU ? BN / 2 : BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
@@ -98,7 +108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, 512);
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
     tmem_relinquish_pair();
   }
   tc_fence_before();
@@ -131,9 +141,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         int b_row;
         if (EPI == EPI_GEGLU) {
           bmap = rank == 0 ? &tmB0 : &tmB1;   // gate rows on the even CTA, up rows on the odd
-          b_row = tn * 128;
+          b_row = tn * (BN / 2);
         } else {
-          b_row = tn * 256 + static_cast<int>(rank) * 128;
+          b_row = tn * BN + static_cast<int>(rank) * (BN / 2);
         }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, status, SITE_PRODUCER_EMPTY, timeout_ns)) {
@@ -164,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(256, kPairBN);
+      constexpr uint32_t idesc = idesc_bf16_f32(256, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -174,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(&tempty[buf], use ^ 1u, status, SITE_MMA_TMEM_EMPTY, timeout_ns)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kPairBN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, status, SITE_MMA_FULL, timeout_ns)) {
             ok = false;
@@ -217,9 +227,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
-                             static_cast<uint32_t>(buf * kPairBN);
+                             static_cast<uint32_t>(buf * BN);
       const int row0 = tm * 256 + static_cast<int>(rank) * 128 + wq * 32;
-      epilogue_cols<kPairBN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
+      epilogue_cols<BN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
                                           &tmY, bias, gelu_mode);
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf * 8));
@@ -233,22 +243,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   cluster_sync();   // the peer's MMAs, loads and arrivals are finished
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, 512);
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
 }
 
-int gemm_tc2_smem_bytes() { return kPairSmem; }
-
-template <int EPI>
+template <int BN, int EPI>
 static cudaError_t launch_pair(const GemmLaunch& L) {
-  auto kern = gemm_tc2_kernel<EPI>;
+  using C = PairCfg<BN>;
+  auto kern = gemm_tc2_kernel<BN, EPI>;
   static SmemAttrCache cache;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kPairSmem, cache);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM, cache);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -266,24 +275,24 @@ static cudaError_t launch_pair(const GemmLaunch& L) {
 
 cudaError_t gemm_tc2_launch(const GemmLaunch& L) {
   if (L.grid < 2 || (L.grid & 1)) return cudaErrorInvalidValue;
-  switch (L.epi) {
-    case EPI_BIAS: return launch_pair<EPI_BIAS>(L);
-    case EPI_BIAS_GELU: return launch_pair<EPI_BIAS_GELU>(L);
-    case EPI_GEGLU: return launch_pair<EPI_GEGLU>(L);
+  switch (L.epi * 1000 + L.bn) {
+    case EPI_BIAS * 1000 + 256: return launch_pair<256, EPI_BIAS>(L);
+    case EPI_BIAS_GELU * 1000 + 256: return launch_pair<256, EPI_BIAS_GELU>(L);
+    case EPI_GEGLU * 1000 + 256: return launch_pair<256, EPI_GEGLU>(L);
     default: return cudaErrorInvalidValue;
   }
 }
 
 // Largest number of co-resident CTA pairs (queried once per device by the host).
 cudaError_t gemm_tc2_max_pairs(int* pairs) {
-  auto kern = gemm_tc2_kernel<EPI_BIAS>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  auto kern = gemm_tc2_kernel<256, EPI_BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PairCfg<256>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.dynamicSmemBytes = PairCfg<256>::SMEM;
   int n = 0;
   e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
   if (e != cudaSuccess) return e;

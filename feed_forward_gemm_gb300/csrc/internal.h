@@ -61,7 +61,6 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L);
 // CTA-pair (cta_group::2) kernel: 256 x 256 tiles over clusters of two CTAs; bn is 256;
 // grid = 2 x pairs.
 cudaError_t gemm_tc2_launch(const GemmLaunch& L);
-int gemm_tc2_smem_bytes();
 cudaError_t gemm_tc2_max_pairs(int* pairs);
 // Dynamic shared memory a GEMM configuration needs (0 if the configuration does not exist).
 int gemm_tc_smem_bytes(int epi, int bn);

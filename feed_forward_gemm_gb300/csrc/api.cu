@@ -350,8 +350,7 @@ int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
 
 fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void* W0,
                         const void* W1, const void* bias, void* y, int64_t T, int64_t K,
-                        int64_t N, int gelu_mode, cudaStream_t s,
-                        const void* next_w = nullptr, size_t next_bytes = 0) {
+                        int64_t N, int gelu_mode, cudaStream_t s) {
   GemvLaunch L;
   L.x = x;
   L.W0 = W0;
@@ -366,10 +365,6 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
   L.grid = gemv_grid(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N),
                      epi == EPI_GEGLU ? 2 : 1, d.sms);
   L.stream = s;
-  const bool warm = next_w != nullptr && next_bytes > 0 && next_bytes <= kGemvNextPrefetchMax &&
-                    next_bytes % 16 == 0;
-  L.next_w = warm ? next_w : nullptr;
-  L.next_bytes = warm ? next_bytes : 0;
   cudaError_t e = gemv_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
   return FMLP_OK;
@@ -556,7 +551,7 @@ fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void
   }
   fmlp_status r;
   if (plan == FMLP_PLAN_GEMV) {
-    r = launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st, Wd, mat_bytes(D, H));
+    r = launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st);
     if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st);
   } else {
     r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
@@ -613,7 +608,7 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
   fmlp_status r;
   if (plan_mlp(T, D, H, Dout, d->sms) == FMLP_PLAN_GEMV) {
     r = launch_gemv(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, D, H, static_cast<int>(mode),
-                    st, W2, mat_bytes(Dout, H));
+                    st);
     if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st);
   } else {
     r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D, static_cast<int>(mode),

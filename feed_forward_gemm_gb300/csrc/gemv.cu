@@ -9,13 +9,11 @@
 //   - the CTA's rows are cut into 512-byte segments (256 weights, one 16-byte vector per
 //     lane) and each warp takes one contiguous run of segments, so every warp streams its own
 //     contiguous range of W with 8 non-allocating 128-bit loads per lane in flight;
-//   - programmatic dependent launch: the kernel lets the next kernel launch at once and
-//     prefetches its weight rows into L2 before waiting for the previous kernel; after the
-//     wait, the first batch of weight loads is issued before x is staged, so the x load hides
-//     under them;
-//   - when the caller names the next layer's weights (the second GEMV of the same block) and
-//     they fit in L2, each CTA also prefetches its share of them into L2, so the second layer
-//     streams them from L2 while HBM serves both layers back to back;
+//   - programmatic dependent launch: the kernel lets the next kernel launch at once; after
+//     waiting for the previous kernel, the first batch of weight loads is issued before x is
+//     staged, so the x load hides under them. (L2 prefetches of the CTA's own rows, or of the
+//     next layer's weights, were measured to slow the decode forward down: they queue ahead
+//     of the loads the warps need first.)
 //   - x (T x K bf16) sits in shared memory; each lane accumulates its dot products in fp32
 //     across the consecutive segments of one row and the warp reduces with shuffles only when
 //     its run crosses a row boundary. The reduced sum of a run piece is stored as the partial
@@ -41,10 +39,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ float dot8(uint4 w, uint4 x, float s) {
@@ -78,16 +72,6 @@ __device__ __forceinline__ void flush_piece(float (&acc)[TMAX], float* part, siz
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
 }
 
-// L2 prefetch of rows [r0, r1) of a [*, K] bf16 matrix.
-__device__ __forceinline__ void prefetch_rows(const __nv_bfloat16* W, int r0, int r1, int K) {
-  const char* base = reinterpret_cast<const char*>(W + static_cast<size_t>(r0) * K);
-  const size_t bytes = static_cast<size_t>(r1 - r0) * K * 2;
-  for (size_t off = 0; off < bytes; off += 65536) {
-    const size_t n = bytes - off < 65536 ? bytes - off : 65536;
-    prefetch_l2_bulk(base + off, static_cast<uint32_t>(n));
-  }
-}
-
 __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -97,9 +81,9 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
 }
 
 // One layer for this CTA's rows [r0, r1) of W (NMAT matrices): y[t, n] for n in [r0, r1).
-// All threads of the CTA take part (it synchronises internally). X_COHERENT reads x through
-// L2 instead of the read-only path (for x written by other CTAs of the same kernel).
-template <int EPI, int NMAT, int TMAX, bool X_COHERENT>
+// All threads of the CTA take part (it synchronises internally). x, which the kernel this one
+// waited for may have written, is read through L2 (never a possibly stale L1 line).
+template <int EPI, int NMAT, int TMAX>
 __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __restrict__ x,
                                           const __nv_bfloat16* __restrict__ W0,
                                           const __nv_bfloat16* __restrict__ W1,
@@ -138,8 +122,7 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
 
   const int xvec = T * (K / 8);
   for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
-    xs[i] = X_COHERENT ? ld_cg_v4(reinterpret_cast<const uint4*>(x) + i)
-                       : __ldg(reinterpret_cast<const uint4*>(x) + i);
+    xs[i] = ld_cg_v4(reinterpret_cast<const uint4*>(x) + i);
   __syncthreads();
 
   float acc[TMAX];
@@ -204,25 +187,12 @@ template <int EPI, int NMAT, int TMAX>
 __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
                 const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode,
-                const char* __restrict__ next_w, size_t next_bytes) {
+                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode) {
   extern __shared__ __align__(16) uint8_t gsm[];
   const int r0 = split_row(blockIdx.x, N), r1 = split_row(blockIdx.x + 1, N);
   if (threadIdx.x == 0) pdl_launch_dependents();
-  // Warm L2 with this CTA's weight rows; they are not produced by the previous kernel.
-  if (threadIdx.x == 0) prefetch_rows(W0, r0, r1, K);
-  if (NMAT == 2 && threadIdx.x == 1) prefetch_rows(W1, r0, r1, K);
-  // This CTA's 1/gridDim share of the next layer's weights (16-byte granules).
-  if (next_w != nullptr && threadIdx.x == 32) {
-    const size_t gran = next_bytes / 16;
-    const size_t b0 = (gran * blockIdx.x) / gridDim.x * 16, b1 = (gran * (blockIdx.x + 1)) / gridDim.x * 16;
-    for (size_t off = b0; off < b1; off += 65536) {
-      const size_t n = b1 - off < 65536 ? b1 - off : 65536;
-      prefetch_l2_bulk(next_w + off, static_cast<uint32_t>(n));
-    }
-  }
   pdl_wait_primary();
-  gemv_rows<EPI, NMAT, TMAX, false>(gsm, x, W0, W1, bias, y, T, K, N, gelu_mode, r0, r1);
+  gemv_rows<EPI, NMAT, TMAX>(gsm, x, W0, W1, bias, y, T, K, N, gelu_mode, r0, r1);
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
@@ -261,8 +231,7 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
                             static_cast<const __nv_bfloat16*>(L.W0),
                             static_cast<const __nv_bfloat16*>(L.W1),
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode,
-                            static_cast<const char*>(L.next_w), L.next_bytes);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode);
 }
 
 cudaError_t gemv_launch(const GemvLaunch& L) {

@@ -80,12 +80,7 @@ struct GemvLaunch {
   int gelu_mode;
   int grid;
   cudaStream_t stream;
-  const void* next_w;   // weights of the next GEMV to warm in L2 (or nullptr)
-  size_t next_bytes;    // their size (a multiple of 16 bytes)
 };
-// Largest next-layer weight block the GEMV warms in L2 (L2 holds 126 MB; this layer's own
-// weights stream through it at the same time).
-constexpr size_t kGemvNextPrefetchMax = size_t(48) << 20;
 // CTAs of the GEMV (nmat weight matrices of [N, K], T tokens) on a device with `sms` SMs.
 int gemv_grid(int T, int K, int N, int nmat, int sms);
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);

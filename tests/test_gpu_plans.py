@@ -191,3 +191,62 @@ def test_decode_repeated_and_on_two_streams():
         assert np.array_equal(o, outs[0])
     assert_parity(outs[0], ref, "decode")
     assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
+
+
+# ------------------------------------------------------------------------ decode ordering
+
+def test_decode_weights_written_by_previous_kernels():
+    """Kernels of a decode block start before the kernel queued ahead of them has finished
+    (programmatic dependent launch); they must still see weights that kernels queued just
+    before the block wrote. W2 of a block is written, on the same stream with no
+    synchronisation, first by a tensor-core Linear and then by the second GEMV of another
+    decode block; both results must match the oracle run on the weights as written."""
+    s = torch.cuda.Stream()
+    # (1) W2 [1024, 2048] is the output of a tensor-core Linear queued right before the block
+    Tl, Kl, Nl = 1024, 256, 2048
+    xl, Wl, bl = rbits((Tl, Kl)), ubits((Nl, Kl), 1 / 16), ubits((Nl,), 1 / 16)
+    assert fm.fmlp_linear_plan(Tl, Kl, Nl) == fm.FMLP_PLAN_TC
+    D, H, Dout = 1024, 2048, 1024
+    x, W1, b1, b2 = rbits((1, D)), ubits((H, D), 1 / 32), ubits((H,), 1 / 32), ubits((Dout,), 1 / 45)
+    dxl, dWl, dbl, dx, dW1, db1, db2 = (to_dev(a) for a in (xl, Wl, bl, x, W1, b1, b2))
+    W2 = torch.zeros((Dout, H), dtype=torch.bfloat16, device="cuda")   # stale contents: zeros
+    y = empty_bf16(1, Dout)
+    ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, D, H, Dout))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        fm.fmlp_linear_bias(dxl, dWl, dbl, W2, Tl, Kl, Nl, stream=s)
+        fm.fmlp_mlp_gelu(dx, dW1, db1, W2, db2, y, 1, D, H, Dout, fm.FMLP_GELU_ERF, ws,
+                         ws.numel(), stream=s)
+    s.synchronize()
+    W2_bits = to_host(W2)
+    assert np.any(W2_bits != 0)
+    assert_parity(to_host(y), oracle.mlp_gelu(x, W1, b1, W2_bits, b2), "decode after linear")
+
+    # (2) W2 of block B [8, 2048] is y [4, 4096] of decode block A, queued right before B
+    TA, DA, HA, DoA = 4, 1024, 2048, 4096
+    xa, W1a, b1a = rbits((TA, DA)), ubits((HA, DA), 1 / 32), ubits((HA,), 1 / 32)
+    W2a, b2a = ubits((DoA, HA), 1 / 45), ubits((DoA,), 1 / 45)
+    DB, HB, DoB = 512, 2048, 8
+    xb, W1b, b1b, b2b = rbits((1, DB)), ubits((HB, DB), 1 / 23), ubits((HB,), 1 / 23), ubits((DoB,), 1 / 45)
+    dA = [to_dev(a) for a in (xa, W1a, b1a, W2a, b2a)]
+    dB = [to_dev(a) for a in (xb, W1b, b1b, b2b)]
+    yA = torch.zeros((TA, DoA), dtype=torch.bfloat16, device="cuda")
+    yB = empty_bf16(1, DoB)
+    wsA = workspace(fm.fmlp_mlp_gelu_workspace_size(TA, DA, HA, DoA))
+    wsB = workspace(fm.fmlp_mlp_gelu_workspace_size(1, DB, HB, DoB))
+    assert fm.fmlp_mlp_gelu_plan(TA, DA, HA, DoA) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == fm.FMLP_PLAN_GEMV
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(3):   # repeated, so that earlier blocks' kernels overlap later ones
+            fm.fmlp_mlp_gelu(dA[0], dA[1], dA[2], dA[3], dA[4], yA, TA, DA, HA, DoA,
+                             fm.FMLP_GELU_ERF, wsA, wsA.numel(), stream=s)
+            fm.fmlp_mlp_gelu(dB[0], dB[1], dB[2], yA.view(DoB, HB), dB[3], yB, 1, DB, HB, DoB,
+                             fm.FMLP_GELU_ERF, wsB, wsB.numel(), stream=s)
+    s.synchronize()
+    yA_bits = to_host(yA)
+    assert_parity(yA_bits, oracle.mlp_gelu(xa, W1a, b1a, W2a, b2a), "decode block A")
+    assert_parity(to_host(yB), oracle.mlp_gelu(xb, W1b, b1b, yA_bits.reshape(DoB, HB), b2b),
+                  "decode block B on A's output")
+    assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
+

@@ -65,14 +65,19 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = q * 8 + e * 2;
-            float z0 = __uint_as_float(a[i]) + bf16_lo(wb[e]);
-            float z1 = __uint_as_float(a[i + 1]) + bf16_hi(wb[e]);
-            if (EPI == EPI_BIAS_GELU) {
-              z0 = gelu_f(z0, gelu_mode);
-              z1 = gelu_f(z1, gelu_mode);
-            }
-            a[i] = __float_as_uint(z0);
-            a[i + 1] = __float_as_uint(z1);
+            a[i] = __float_as_uint(__uint_as_float(a[i]) + bf16_lo(wb[e]));
+            a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
+          }
+        }
+        // the GELU flavour is chosen once per 32 columns, so the 32 evaluations are
+        // independent straight-line code the scheduler can overlap
+        if (EPI == EPI_BIAS_GELU) {
+          if (gelu_mode == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_erf_f(__uint_as_float(a[i])));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])));
           }
         }
       }

@@ -6,7 +6,7 @@ fmlp_oracle.c (plain loops, double precision, bf16 rounding only where the fused
 rounds); this wrapper only marshals numpy arrays of bf16 bit patterns.
 
 Parity pins (tests/test_oracle.py): GELU against the normal CDF table and torch's fp64
-GELU, the page's nn.Linear layout worked example, identity/zero weights, special cases with
+GELU, ReLU against torch's relu, the page's nn.Linear layout worked example, identity/zero weights, special cases with
 distinguishable operands, rounding against an independent exact rounding, and brute force
 against torch's fp64 nn.Linear / F.gelu on tiny shapes. No function here is unpinned.
 """
@@ -27,6 +27,7 @@ _lib = None
 
 GELU_TANH = 0
 GELU_ERF = 1
+RELU = 2        # the MLP's hidden activation may also be ReLU
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64

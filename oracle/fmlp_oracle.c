@@ -83,8 +83,14 @@ static double gelu_erf(double x) {
     return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
 }
 
-/* mode 0 = tanh approximation, 1 = exact (erf) */
-static double gelu(double x, int mode) { return mode == 1 ? gelu_erf(x) : gelu_tanh(x); }
+/* ReLU, the hidden activation of the two-layer MLP of the ainews.cool article's technical
+ * deep-dive: max(x, 0), with NaN passed through (as torch's relu does) and -0 giving +0. */
+static double relu(double x) { return x > 0.0 ? x : (x != x ? x : 0.0); }
+
+/* mode 0 = GELU tanh approximation, 1 = exact GELU (erf), 2 = ReLU */
+static double gelu(double x, int mode) {
+    return mode == 2 ? relu(x) : (mode == 1 ? gelu_erf(x) : gelu_tanh(x));
+}
 
 void oracle_gelu(const double* in, double* out, int64_t n, int mode) {
     for (int64_t i = 0; i < n; ++i) out[i] = gelu(in[i], mode);
@@ -223,7 +229,7 @@ int oracle_linear(const uint16_t* x, const uint16_t* W, const uint16_t* b, uint1
 }
 
 /* h = bf16(GELU(x W1^T + b1)); y = bf16(h W2^T + b2). b1, b2 may be NULL.
- * gelu_mode: 0 tanh, 1 erf. h_out (nullable) receives h as bf16 bits [nrows, H]. */
+ * gelu_mode: 0 GELU tanh, 1 GELU erf, 2 ReLU. h_out (nullable) receives h as bf16 bits [nrows, H]. */
 int oracle_mlp_gelu(const uint16_t* x, const uint16_t* W1, const uint16_t* b1,
                     const uint16_t* W2, const uint16_t* b2, uint16_t* y, double* y_acc,
                     uint16_t* h_out, int64_t T, int64_t D, int64_t H, int64_t Dout,

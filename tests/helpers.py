@@ -66,7 +66,8 @@ def torch_geglu_f64(x, Wg, Wu, Wd, round_m: bool = True):
 def torch_mlp_f64(x, W1, b1, W2, b2, approximate: str):
     xf, w1, w2 = t64(x), t64(W1), t64(W2)
     z = torch.nn.functional.linear(xf, w1, None if b1 is None else t64(b1))
-    h = torch.nn.functional.gelu(z, approximate=approximate).numpy()
+    h = (torch.relu(z) if approximate == "relu"
+         else torch.nn.functional.gelu(z, approximate=approximate)).numpy()
     h_bits = rne_bf16_array(h)
     y = torch.nn.functional.linear(torch.from_numpy(bits_to_f64(h_bits)), w2,
                                    None if b2 is None else t64(b2))

@@ -197,7 +197,19 @@ def test_geglu_eager_and_fused_rounding_both_within_tolerance():
 
 # ---------------------------------------------------------------------------- MLP
 
-@pytest.mark.parametrize("approx,mode", [("tanh", oracle.GELU_TANH), ("none", oracle.GELU_ERF)])
+def test_relu_matches_torch():
+    xs = np.array([-3.5, -1e-300, -0.0, 0.0, 1e-300, 0.25, 7.0, 1e300, -1e300, np.inf, -np.inf,
+                   np.nan])
+    got = oracle.gelu(xs, oracle.RELU)
+    ref = torch.relu(torch.from_numpy(xs)).numpy()
+    assert np.array_equal(got, ref, equal_nan=True)
+    assert not np.signbit(got[2])                 # relu(-0) is +0
+    rnd = np.random.default_rng(5).standard_normal(10000) * 4
+    assert np.array_equal(oracle.gelu(rnd, oracle.RELU), np.maximum(rnd, 0.0))
+
+
+@pytest.mark.parametrize("approx,mode", [("tanh", oracle.GELU_TANH), ("none", oracle.GELU_ERF),
+                                         ("relu", oracle.RELU)])
 @pytest.mark.parametrize("T,D,H,Do", [(1, 8, 16, 8), (17, 32, 72, 16), (129, 16, 32, 24)])
 def test_mlp_brute_force_vs_torch(approx, mode, T, D, H, Do):
     x = rand_bits((T, D))
@@ -215,10 +227,12 @@ def test_mlp_identity_weights():
     x = rand_bits((30, D))
     b1, b2 = rand_bits((D,), 0.5), rand_bits((D,), 0.5)
     eye = rne_bf16_array(np.eye(D))
-    for approx, mode in (("tanh", oracle.GELU_TANH), ("none", oracle.GELU_ERF)):
+    for approx, mode in (("tanh", oracle.GELU_TANH), ("none", oracle.GELU_ERF),
+                         ("relu", oracle.RELU)):
         y = oracle.mlp_gelu(x, eye, b1, eye, b2, gelu_mode=mode)
         z = torch.from_numpy(bits_to_f64(x) + bits_to_f64(b1)[None, :])
-        h = bits_to_f64(rne_bf16_array(torch.nn.functional.gelu(z, approximate=approx).numpy()))
+        act = torch.relu(z) if approx == "relu" else torch.nn.functional.gelu(z, approximate=approx)
+        h = bits_to_f64(rne_bf16_array(act.numpy()))
         assert np.array_equal(y, rne_bf16_array(h + bits_to_f64(b2)[None, :]))
     # bias-free and zero first layer: y = b2
     y0 = oracle.mlp_gelu(x, np.zeros((D, D), np.uint16), None, eye, b2)

@@ -389,14 +389,17 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     wsb = fm.fmlp_mlp_gelu_workspace_size(w.T, w.D, w.H, w.Dout)
     ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
 
-    def mlp():
-        fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, w.T, w.D, w.H, w.Dout,
-                         fm.FMLP_GELU_ERF, ws, wsb, stream)
-    ms = cold_time(mlp, 30)
-    out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
-                   "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                   "plan": fm.fmlp_mlp_gelu_plan(w.T, w.D, w.H, w.Dout),
-                   "l2": "flushed before every call (median of 30)"}
+    for name, mode in ((w.name, fm.FMLP_GELU_ERF), (w.name + "_relu", fm.FMLP_RELU)):
+        def mlp(mode=mode):
+            fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, w.T, w.D, w.H,
+                             w.Dout, mode, ws, wsb, stream)
+        ms = cold_time(mlp, 30)
+        out[name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
+                     "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                              4),
+                     "activation": "gelu_erf" if mode == fm.FMLP_GELU_ERF else "relu",
+                     "plan": fm.fmlp_mlp_gelu_plan(w.T, w.D, w.H, w.Dout),
+                     "l2": "flushed before every call (median of 30)"}
     del d, y, ws
 
     # the same MLP at one token (decode): weights rotate through 5 copies (336 MB > 2x L2)

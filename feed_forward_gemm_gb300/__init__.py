@@ -32,7 +32,7 @@ __all__ = [
 
 FMLP_OK, FMLP_ERR_NULL, FMLP_ERR_SHAPE, FMLP_ERR_ALIGN, FMLP_ERR_ALIAS = 0, 1, 2, 3, 4
 FMLP_ERR_WORKSPACE, FMLP_ERR_CUDA, FMLP_ERR_DEVICE_TIMEOUT, FMLP_ERR_DEVICE = 5, 6, 7, 8
-FMLP_GELU_TANH, FMLP_GELU_ERF = 0, 1
+FMLP_GELU_TANH, FMLP_GELU_ERF, FMLP_RELU = 0, 1, 2
 FMLP_PLAN_NONE, FMLP_PLAN_TC, FMLP_PLAN_FUSED_SMALL, FMLP_PLAN_GEMV = 0, 1, 2, 3
 FMLP_TILES_AUTO, FMLP_TILES_SINGLE, FMLP_TILES_PAIR = 0, 1, 2
 

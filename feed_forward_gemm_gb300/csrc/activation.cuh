@@ -34,8 +34,12 @@ __device__ __forceinline__ float gelu_erf_f(float x) {
   return 0.5f * x * (x >= 0.0f ? 2.0f - q : q);
 }
 
+// ReLU: max(x, 0), NaN passed through, -0 giving +0 (as torch's relu).
+__device__ __forceinline__ float relu_f(float x) { return x > 0.0f ? x : (x != x ? x : 0.0f); }
+
+// The hidden activation by mode: 0 GELU tanh, 1 GELU erf, 2 ReLU.
 __device__ __forceinline__ float gelu_f(float x, int mode) {
-  return mode == 1 ? gelu_erf_f(x) : gelu_tanh_f(x);
+  return mode == 2 ? relu_f(x) : (mode == 1 ? gelu_erf_f(x) : gelu_tanh_f(x));
 }
 
 // Two floats -> packed bf16x2 (round to nearest even); `lo` lands in the low half.

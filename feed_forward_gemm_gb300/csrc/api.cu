@@ -27,6 +27,10 @@ __device__ int g_device_status;
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per wait
+
+bool act_mode_ok(int mode) {
+  return mode == FMLP_GELU_TANH || mode == FMLP_GELU_ERF || mode == FMLP_RELU;
+}
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 2147483647;
 
@@ -454,8 +458,8 @@ static fmlp_status linear_common(const void* x, const void* W, const void* b, vo
   FMLP_TRY(check_T(T));
   FMLP_TRY(check_inner(in, "in"));
   FMLP_TRY(check_inner(out, "out"));
-  if (epi == EPI_BIAS_GELU && mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
-    set_error("gelu mode %d is not FMLP_GELU_TANH or FMLP_GELU_ERF", mode);
+  if (epi == EPI_BIAS_GELU && !act_mode_ok(mode)) {
+    set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU", mode);
     return FMLP_ERR_SHAPE;
   }
   if (T == 0) return FMLP_OK;
@@ -573,8 +577,9 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
   FMLP_TRY(check_inner(Dout, "Dout"));
-  if (mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
-    set_error("gelu mode %d is not FMLP_GELU_TANH or FMLP_GELU_ERF", static_cast<int>(mode));
+  if (!act_mode_ok(mode)) {
+    set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU",
+              static_cast<int>(mode));
     return FMLP_ERR_SHAPE;
   }
   if (T == 0) return FMLP_OK;
@@ -710,8 +715,8 @@ fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mod
     set_error("n = %lld < 0", static_cast<long long>(n));
     return FMLP_ERR_SHAPE;
   }
-  if (mode != FMLP_GELU_TANH && mode != FMLP_GELU_ERF) {
-    set_error("gelu mode %d invalid", static_cast<int>(mode));
+  if (!act_mode_ok(mode)) {
+    set_error("activation mode %d invalid", static_cast<int>(mode));
     return FMLP_ERR_SHAPE;
   }
   if (n == 0) return FMLP_OK;

@@ -13,7 +13,7 @@
 // different bank groups) and lane 0 stores the tile with one TMA store. Two staging tiles
 // alternate so the store of one chunk overlaps the math of the next.
 //   EPI_BIAS       v = acc + b
-//   EPI_BIAS_GELU  v = gelu(acc + b)
+//   EPI_BIAS_GELU  v = act(acc + b), act = GELU (tanh or erf) or ReLU
 //   EPI_GEGLU      v = gelu_tanh(acc[c]) * acc[c + BN/2]  (gate columns, then up columns)
 #pragma once
 
@@ -69,12 +69,15 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
             a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
           }
         }
-        // the GELU flavour is chosen once per 32 columns, so the 32 evaluations are
+        // the activation is chosen once per 32 columns, so the 32 evaluations are
         // independent straight-line code the scheduler can overlap
         if (EPI == EPI_BIAS_GELU) {
           if (gelu_mode == 1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_erf_f(__uint_as_float(a[i])));
+          } else if (gelu_mode == 2) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(relu_f(__uint_as_float(a[i])));
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])));

@@ -76,10 +76,11 @@ typedef enum {
     FMLP_ERR_DEVICE = 8
 } fmlp_status;
 
-/* GELU flavour. TANH: 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))), the
- * approximate="tanh" form of section "Stacking three Linears: the MLP". ERF: the exact
- * 0.5 x (1 + erf(x / sqrt 2)), nn.GELU's default. */
-typedef enum { FMLP_GELU_TANH = 0, FMLP_GELU_ERF = 1 } fmlp_gelu_mode;
+/* Hidden activation of the MLP calls. GELU_TANH: 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))),
+ * the approximate="tanh" form of section "Stacking three Linears: the MLP". GELU_ERF: the exact
+ * 0.5 x (1 + erf(x / sqrt 2)), nn.GELU's default. RELU: max(x, 0) (NaN passed through, -0
+ * giving +0), the activation of the ainews.cool article's two-layer MLP. */
+typedef enum { FMLP_GELU_TANH = 0, FMLP_GELU_ERF = 1, FMLP_RELU = 2 } fmlp_gelu_mode;
 
 /* Which kernel sequence a call with these sizes runs (reported by the *_plan queries). */
 typedef enum {
@@ -95,8 +96,8 @@ typedef enum {
 FMLP_API fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y,
                              int64_t T, int64_t in, int64_t out, fmlp_stream_t s);
 
-/* h[T, out] = bf16(GELU(x[T, in] @ W[out, in]^T + b[out])), GELU per `mode`, b nullable.
- * The first half of fmlp_mlp_gelu as its own call (bias+GELU epilogue). */
+/* h[T, out] = bf16(act(x[T, in] @ W[out, in]^T + b[out])), act = GELU or ReLU per `mode`, b
+ * nullable. The first half of fmlp_mlp_gelu as its own call (bias+activation epilogue). */
 FMLP_API fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,
                                   int64_t T, int64_t in, int64_t out, fmlp_gelu_mode mode,
                                   fmlp_stream_t s);
@@ -116,7 +117,8 @@ FMLP_API fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, c
                        int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
                        fmlp_stream_t s);
 
-/* y[T, Dout] = bf16(h W2[Dout, H]^T + b2) with h = bf16(GELU(x[T, D] W1[H, D]^T + b1)).
+/* y[T, Dout] = bf16(h W2[Dout, H]^T + b2) with h = bf16(act(x[T, D] W1[H, D]^T + b1)), act =
+ * GELU (tanh or erf) or ReLU per `mode`.
  * b1, b2 nullable. ws as for fmlp_geglu, sized by fmlp_mlp_gelu_workspace_size(). */
 FMLP_API fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const void* W2,
                           const void* b2, void* y, int64_t T, int64_t D, int64_t H,
@@ -169,8 +171,8 @@ FMLP_API fmlp_status fmlp_set_tile_policy(int policy);
 FMLP_API fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t Dout,
                                         char* buf, size_t buflen);
 
-/* Device activation check: out[i] = GELU(in[i]) in fp32 with the exact device code the
- * epilogues use. in/out: n floats in device memory. One kernel. */
+/* Device activation check: out[i] = act(in[i]) (GELU or ReLU per mode) in fp32 with the exact
+ * device code the epilogues use. in/out: n floats in device memory. One kernel. */
 FMLP_API fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp_gelu_mode mode,
                            fmlp_stream_t s);
 

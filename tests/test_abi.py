@@ -118,6 +118,8 @@ def test_mlp_validation(lib):
                                 stream=0, raise_on_error=False)
     assert call(W2=0) == fm.FMLP_ERR_NULL
     assert call(mode=7) == fm.FMLP_ERR_SHAPE
+    assert call(mode=3, T=0) == fm.FMLP_ERR_SHAPE          # checked before the T == 0 exit
+    assert call(mode=fm.FMLP_RELU, T=0) == fm.FMLP_OK
     assert call(Do=6) == fm.FMLP_ERR_SHAPE
     assert call(y=A + 4 * GB) == fm.FMLP_ERR_ALIAS          # y on top of b2
     assert call(T=0) == fm.FMLP_OK
@@ -134,6 +136,10 @@ def test_gelu_eval_and_timeout_validation(lib):
     assert fm.fmlp_gelu_eval(A, A + GB, 4, mode=3, stream=0,
                              raise_on_error=False) == fm.FMLP_ERR_SHAPE
     assert fm.fmlp_gelu_eval(0, 0, 0, stream=0, raise_on_error=False) == fm.FMLP_OK
+    assert fm.fmlp_gelu_eval(0, 0, 0, mode=fm.FMLP_RELU, stream=0,
+                             raise_on_error=False) == fm.FMLP_OK
+    assert fm.fmlp_linear_bias_gelu(A, A + GB, None, A + 2 * GB, 8, 32, 64, 3, stream=0,
+                                    raise_on_error=False) == fm.FMLP_ERR_SHAPE
     assert fm.fmlp_test_wait_timeout(0, stream=0, raise_on_error=False) == fm.FMLP_ERR_SHAPE
 
 

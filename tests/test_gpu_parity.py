@@ -54,6 +54,22 @@ def test_device_gelu_matches_oracle(mode):
     assert np.abs(got - other).max() > 1e-4
 
 
+def test_device_relu_is_exact():
+    xs = np.concatenate([np.array([-0.0, 0.0, 1e-38, -1e-38, 3.5, -3.5, 1e38, -1e38,
+                                   np.inf, -np.inf, np.nan]),
+                         rng.standard_normal(20000) * 3]).astype(np.float32)
+    din = torch.from_numpy(xs).to(DEV)
+    dout = torch.empty_like(din)
+    fm.fmlp_gelu_eval(din, dout, xs.size, fm.FMLP_RELU)
+    got = dout.cpu().numpy()
+    ref = oracle.gelu(xs.astype(np.float64), oracle.RELU).astype(np.float32)
+    # NaN stays NaN (its payload is not part of ReLU's definition); everything else bit for bit
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    bad = np.flatnonzero(got[ok].view(np.uint32) != ref[ok].view(np.uint32))
+    assert bad.size == 0, (xs[ok][bad[:5]], got[ok][bad[:5]], ref[ok][bad[:5]])
+
+
 # ------------------------------------------------------------------------ Linear + bias
 
 LINEAR_SHAPES = [
@@ -104,7 +120,7 @@ def test_linear_layout_worked_example_padded():
     assert bits_to_f64(to_host(y))[0, :3].tolist() == [11.0, 33.0, 55.0]
 
 
-@pytest.mark.parametrize("mode", [fm.FMLP_GELU_TANH, fm.FMLP_GELU_ERF])
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_TANH, fm.FMLP_GELU_ERF, fm.FMLP_RELU])
 @pytest.mark.parametrize("T,K,N", [(1, 64, 64), (129, 96, 520), (513, 512, 384)])
 def test_linear_bias_gelu_vs_oracle(mode, T, K, N):
     x, W, b = rbits((T, K)), ubits((N, K), 1 / math.sqrt(K)), ubits((N,), 1 / math.sqrt(K))
@@ -113,9 +129,8 @@ def test_linear_bias_gelu_vs_oracle(mode, T, K, N):
     torch.cuda.synchronize()
     # reference h: the oracle's MLP intermediate with an identity second layer
     _, ref_h = oracle.mlp_gelu(x, W, b, rne_bf16_array(np.eye(N)), None,
-                               gelu_mode=oracle.GELU_TANH if mode == 0 else oracle.GELU_ERF,
-                               want_h=True)
-    assert_parity(to_host(h), ref_h, "linear+bias+gelu")
+                               gelu_mode={0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode], want_h=True)
+    assert_parity(to_host(h), ref_h, "linear+bias+activation")
 
 
 # ------------------------------------------------------------------------ GeGLU
@@ -201,7 +216,7 @@ def test_geglu_deterministic_and_row_permutation_equivariant():
 
 # ------------------------------------------------------------------------ Linear -> GELU -> Linear
 
-@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH])
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH, fm.FMLP_RELU])
 @pytest.mark.parametrize("T,D,H,Do", [(1, 64, 128, 64), (5, 256, 256, 256), (130, 64, 192, 72),
                                       (700, 512, 1024, 256)])
 def test_mlp_gelu_vs_oracle(mode, T, D, H, Do):
@@ -214,9 +229,8 @@ def test_mlp_gelu_vs_oracle(mode, T, D, H, Do):
                      mode, ws, ws.numel())
     torch.cuda.synchronize()
     check()
-    ref = oracle.mlp_gelu(x, W1, b1, W2, b2,
-                          gelu_mode=oracle.GELU_TANH if mode == 0 else oracle.GELU_ERF)
-    assert_parity(to_host(y), ref, f"mlp {T}x{D}x{H}x{Do}")
+    ref = oracle.mlp_gelu(x, W1, b1, W2, b2, gelu_mode={0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode])
+    assert_parity(to_host(y), ref, f"mlp {T}x{D}x{H}x{Do} mode {mode}")
 
 
 def test_mlp_without_biases():

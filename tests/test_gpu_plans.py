@@ -107,7 +107,7 @@ def test_gemv_geglu_vs_oracle(T, D, H):
     assert_parity(to_host(m), ref_m, "gemv gate/up")
 
 
-@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH])
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH, fm.FMLP_RELU])
 def test_decode_mlp_4096_vs_oracle(mode):
     w = synth.WORKLOADS["mlp_4096_t1"]
     assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == fm.FMLP_PLAN_GEMV
@@ -120,8 +120,8 @@ def test_decode_mlp_4096_vs_oracle(mode):
     torch.cuda.synchronize()
     check()
     ref = oracle.mlp_gelu(t["x"], t["W1"], t["b1"], t["W2"], t["b2"],
-                          gelu_mode=oracle.GELU_ERF if mode == fm.FMLP_GELU_ERF else oracle.GELU_TANH)
-    assert_parity(to_host(y), ref, "decode mlp 4096")
+                          gelu_mode={0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode])
+    assert_parity(to_host(y), ref, f"decode mlp 4096 mode {mode}")
 
 
 def test_gemv_deterministic_across_calls():

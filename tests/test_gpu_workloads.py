@@ -47,7 +47,7 @@ def test_70b_class_geglu_sampled_rows():
     assert np.isfinite(y.view(np.int16)).all()
 
 
-@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH])
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH, fm.FMLP_RELU])
 def test_mlp_4096_at_4096_tokens(mode):
     w = synth.WORKLOADS["mlp_4096_t4096"]
     t = w.generate()
@@ -57,7 +57,7 @@ def test_mlp_4096_at_4096_tokens(mode):
     fm.fmlp_mlp_gelu(d["x"], d["W1"], d["b1"], d["W2"], d["b2"], y, w.T, w.D, w.H, w.Dout, mode,
                      ws, ws.numel())
     torch.cuda.synchronize()
-    om = oracle.GELU_ERF if mode == fm.FMLP_GELU_ERF else oracle.GELU_TANH
+    om = {0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode]
     rows = None if mode == fm.FMLP_GELU_ERF else sample_rows(w.T)
     ref = oracle.mlp_gelu(t["x"], t["W1"], t["b1"], t["W2"], t["b2"], gelu_mode=om, rows=rows)
     got = to_host(y) if rows is None else to_host(y)[rows]

@@ -280,9 +280,57 @@ GemmChoice choose_gemm(const DeviceState& d, int epi, int64_t M, int64_t N_out) 
   return c;
 }
 
+// The few-token kernel (weights as the MMA's M side, K split over a cluster) serves M <= 128
+// under the automatic tile policy.
+bool use_skinny(int64_t M) {
+  return M >= 1 && M <= kSkinnyMaxT &&
+         g_tile_policy.load(std::memory_order_relaxed) == FMLP_TILES_AUTO;
+}
+
+// K slices per 128-row weight tile: the largest power of two <= 8 that keeps tiles * S within
+// the SM count and gives every slice at least one 64-deep K step.
+int skinny_split(const DeviceState& d, int64_t N_out, int64_t K) {
+  const int64_t tiles = (N_out + 127) / 128, num_kb = (K + 63) / 64;
+  int S = 1;
+  while (S < 8 && tiles * S * 2 <= d.sms && S * 2 <= num_kb) S *= 2;
+  return S;
+}
+
+fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const void* B0,
+                          const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
+                          int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
+  SkinnyLaunch L;
+  memset(&L, 0, sizeof L);
+  L.tpad = static_cast<int>((M + 31) / 32 * 32);
+  FMLP_TRY(make_map(&L.tmW0, B0, N_out, K, 128, "W"));
+  if (epi == EPI_GEGLU) {
+    FMLP_TRY(make_map(&L.tmW1, B1, N_out, K, 128, "W_up"));
+  } else {
+    L.tmW1 = L.tmW0;
+  }
+  FMLP_TRY(make_map(&L.tmX, A, M, K, static_cast<uint32_t>(L.tpad), "x"));
+  L.bias = bias;
+  L.y = Y;
+  L.T = static_cast<int>(M);
+  L.N = static_cast<int>(N_out);
+  L.K = static_cast<int>(K);
+  L.tiles = static_cast<int>((N_out + 127) / 128);
+  L.split = skinny_split(d, N_out, K);
+  L.epi = epi;
+  L.gelu_mode = gelu_mode;
+  L.pdl = pdl;
+  L.stream = s;
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
+  const cudaError_t e = gemm_skinny_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_skinny launch");
+  return FMLP_OK;
+}
+
 fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
                         const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
                         int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
+  if (use_skinny(M)) return launch_skinny(d, epi, A, B0, B1, bias, Y, M, N_out, K, gelu_mode, pdl, s);
   GemmLaunch L;
   memset(&L, 0, sizeof L);
   const bool geglu = epi == EPI_GEGLU;
@@ -320,6 +368,15 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
 // smem bound depends on the grid only through rows per CTA, and GB300 has 152 SMs.
 constexpr int kPlanSms = 152;
 
+// Decode crossover, measured on GB300 (CUDA graphs of 20 calls over 5 weight sets): the GEMV
+// wins at one token, and at two when the call's weights are small (16 MiB or less: 9.3 vs
+// 10.1 us for the GPT-2-small-shaped GeGLU); otherwise the few-token tcgen05 kernel wins
+// (4096-wide MLP at 2-4 tokens: 20.3 us against 25.9-33.9 us for the GEMV).
+constexpr int64_t kGemvSmallWeights = int64_t(16) << 20;
+bool gemv_preferred(int64_t T, int64_t weight_bytes) {
+  return T == 1 || (T == 2 && weight_bytes <= kGemvSmallWeights);
+}
+
 bool gemv_ok(int64_t T, int64_t K, int64_t N, int nmat, int sms) {
   if (T < 1 || T > kGemvMaxT || K % 256 != 0) return false;
   const int grid = gemv_grid(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), nmat,
@@ -330,12 +387,15 @@ bool gemv_ok(int64_t T, int64_t K, int64_t N, int nmat, int sms) {
 
 int plan_linear(int64_t T, int64_t in, int64_t out, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
-  return gemv_ok(T, in, out, 1, sms) ? FMLP_PLAN_GEMV : FMLP_PLAN_TC;
+  return gemv_ok(T, in, out, 1, sms) && gemv_preferred(T, mat_bytes(out, in)) ? FMLP_PLAN_GEMV
+                                                                              : FMLP_PLAN_TC;
 }
 
 int plan_mlp(int64_t T, int64_t D, int64_t H, int64_t Dout, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
-  if (gemv_ok(T, D, H, 1, sms) && gemv_ok(T, H, Dout, 1, sms)) return FMLP_PLAN_GEMV;
+  if (gemv_ok(T, D, H, 1, sms) && gemv_ok(T, H, Dout, 1, sms) &&
+      gemv_preferred(T, mat_bytes(H, D) + mat_bytes(Dout, H)))
+    return FMLP_PLAN_GEMV;
   return FMLP_PLAN_TC;
 }
 
@@ -345,7 +405,9 @@ int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
   const bool gemv_shape = T <= kGemvMaxT && D % 256 == 0 && H % 256 == 0;
   if (gemv_shape) {
-    if (gemv_ok(T, D, H, 2, sms) && gemv_ok(T, H, D, 1, sms)) return FMLP_PLAN_GEMV;
+    if (gemv_ok(T, D, H, 2, sms) && gemv_ok(T, H, D, 1, sms) &&
+        gemv_preferred(T, 3 * mat_bytes(H, D)))
+      return FMLP_PLAN_GEMV;
     return FMLP_PLAN_TC;
   }
   if (D <= kSmallMaxD && D % 16 == 0 && H <= kSmallMaxH) return FMLP_PLAN_FUSED_SMALL;
@@ -511,7 +573,7 @@ fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, vo
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
-  if (gemv_ok(T, D, H, 2, d->sms))
+  if (gemv_ok(T, D, H, 2, d->sms) && gemv_preferred(T, 2 * mat_bytes(H, D)))
     return launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st);
   return launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
 }
@@ -630,6 +692,16 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
 
 static std::string describe_gemm(const DeviceState& d, const char* name, int epi, int64_t M,
                                  int64_t N, int64_t K) {
+  if (use_skinny(M)) {
+    char b[256];
+    snprintf(b, sizeof b,
+             "%s: tcgen05 few-token kernel, 128 weight rows x %lld tokens per tile, K split %d "
+             "ways over a cluster, M=%lld N=%lld K=%lld, grid=%lld",
+             name, static_cast<long long>((M + 31) / 32 * 32), skinny_split(d, N, K),
+             static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+             static_cast<long long>((N + 127) / 128 * skinny_split(d, N, K)));
+    return b;
+  }
   const GemmChoice c = choose_gemm(d, epi, M, N);
   char b[256];
   if (c.pair)
@@ -671,7 +743,8 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
     r = plan_linear(T, D, H, d->sms) == FMLP_PLAN_GEMV ? describe_gemv(*d, "linear", T, D, H)
                                                        : describe_gemm(*d, "linear", epi, T, H, D);
   } else if (op == 2) {              // gate/up
-    r = gemv_ok(T, D, H, 2, d->sms) ? describe_gemv(*d, "gate/up", T, D, H, 2)
+    r = gemv_ok(T, D, H, 2, d->sms) && gemv_preferred(T, 2 * mat_bytes(H, D))
+            ? describe_gemv(*d, "gate/up", T, D, H, 2)
                                     : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
   } else if (op == 3) {              // geglu block
     const int p = plan_geglu(T, D, H, d->sms);

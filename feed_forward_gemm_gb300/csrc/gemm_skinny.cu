@@ -1,0 +1,269 @@
+// tcgen05 GEMM for few tokens (5..128): y[T, N] = epi(x[T, K] W[N, K]^T), weights as the M side.
+//
+// With T <= 128 the usual tiling (128 token rows per tile) leaves most of the MMA's M rows
+// padding and, worse, has only N / BN tiles to spread over the SMs, so a few dozen SMs stream
+// all the weights. At these sizes the block is bound by reading the weights once ("ainews.cool
+// fused-MLP article", technical deep-dive: small-batch inference is limited by memory
+// traffic and launches), so this kernel turns the product around and splits it along K:
+//   - the MMA computes D[n, t] = sum_k W[n, k] x[t, k]: A = 128 weight rows (K-major, the
+//     nn.Linear layout as stored), B = the T tokens padded to Tpad (a multiple of 32, rows past
+//     T read as zeros by TMA), M = 128, N = Tpad, K = 16 per instruction; every byte of each
+//     16 KB A stage is a weight;
+//   - a 128-row weight tile is cut into S K slices (S = 1, 2, 4 or 8) computed by the S CTAs
+//     of one thread-block cluster, so tiles * S CTAs stream the weights at once;
+//   - each CTA parks its fp32 slice D_s[128 x Tpad] in its own shared memory (the stage ring,
+//     no longer needed), the cluster synchronises, and CTA r adds rows [r*128/S, (r+1)*128/S)
+//     of all S slices read through distributed shared memory in slice order s = 0..S-1 (the
+//     same order on every run), applies the epilogue (bias, GELU/ReLU, or gelu_tanh(g)*u for
+//     the GeGLU gate/up pair, whose two accumulators share the B tile) and writes y[t, n].
+// No global scratch, no atomics, no CTA waiting on another outside the cluster barrier,
+// which the hardware provides (the CTAs of a cluster are co-scheduled).
+//
+// Warp roles (one CTA per SM, 6 warps): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer (one thread), warps 2-5 move the accumulator from TMEM to shared memory; all six
+// warps share the cluster reduction. All mbarrier waits are bounded; every thread reaches both
+// cluster barriers whatever happens, so a timeout unwinds without a hang.
+#include "activation.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmlp {
+
+namespace {
+
+constexpr int kSkThreads = 192;
+constexpr int kSkBK = 64;                   // K per stage: one 128-byte swizzle row
+constexpr int kSkRows = 128;                // weight rows per tile (MMA M)
+constexpr int kSkA = kSkRows * kSkBK * 2;   // 16 KB of weights per matrix per stage
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+}  // namespace
+
+// NMAT = 2: GeGLU gate/up (W0 = Wg, W1 = Wu), two accumulators of Tpad columns each.
+template <int EPI, int NMAT>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW0,
+                       const __grid_constant__ CUtensorMap tmW1,
+                       const __grid_constant__ CUtensorMap tmX,
+                       const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ y,
+                       int T, int N, int K, int Tpad, int stages, int gelu_mode, int* status,
+                       uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int b_bytes = Tpad * kSkBK * 2;
+  const int stage_bytes = NMAT * kSkA + b_bytes;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + stages * stage_bytes);
+  uint64_t* empty = full + stages;
+  uint64_t* tfull = empty + stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  // after the main loop the ring holds this CTA's slice: [mat][t][128 rows] fp32
+  float* part = reinterpret_cast<float*>(ring);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = static_cast<int>(cluster_nctarank());   // K slices of the tile
+  const int s = static_cast<int>(cluster_ctarank());
+  const int tile = blockIdx.x / S;
+  const int n0 = tile * kSkRows;
+  const int num_kb = (K + kSkBK - 1) / kSkBK;
+  const int kb0 = s * num_kb / S, kb1 = (s + 1) * num_kb / S;
+  const uint32_t tmem_cols = NMAT * Tpad <= 32 ? 32u : (NMAT * Tpad <= 64 ? 64u
+                             : (NMAT * Tpad <= 128 ? 128u : 256u));
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmW0);
+    if (NMAT == 2) prefetch_tmap(&tmW1);
+    prefetch_tmap(&tmX);
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(tfull, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  pdl_wait_primary();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, status, SITE_PRODUCER_EMPTY, timeout_ns)) break;
+        uint8_t* st = ring + stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
+        tma_load_2d(st, &tmW0, &full[stage], kb * kSkBK, n0);
+        if (NMAT == 2) tma_load_2d(st + kSkA, &tmW1, &full[stage], kb * kSkBK, n0);
+        tma_load_2d(st + NMAT * kSkA, &tmX, &full[stage], kb * kSkBK, 0);
+        if (++stage == stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kSkRows, static_cast<uint32_t>(Tpad));
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, status, SITE_MMA_FULL, timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(ring + stage * stage_bytes);
+        const uint64_t b_desc = sdesc_kmajor_sw128(a_addr + NMAT * kSkA);
+#pragma unroll
+        for (int mat = 0; mat < NMAT; ++mat) {
+          const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + mat * kSkA);
+#pragma unroll
+          for (int kk = 0; kk < kSkBK / 16; ++kk)
+            tc_mma_bf16(tmem_base + static_cast<uint32_t>(mat * Tpad), a_desc + 2u * kk,
+                        b_desc + 2u * kk, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      tc_commit(tfull);   // fires once every MMA issued above has completed
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ TMEM -> shared memory
+    const int wq = warp & 3;   // this warp may read TMEM lanes [32 wq, 32 wq + 32)
+    const bool ok = mbar_wait(tfull, 0, status, SITE_EPI_TMEM_FULL, timeout_ns);
+    __syncwarp();
+    tc_fence_after();
+    if (__all_sync(0xffffffffu, ok)) {
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+      const int row = wq * 32 + lane;
+      for (int mat = 0; mat < NMAT; ++mat) {
+        for (int c = 0; c < Tpad; c += 32) {
+          uint32_t a[32];
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(mat * Tpad + c), a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            part[(static_cast<size_t>(mat) * Tpad + c + j) * kSkRows + row] = __uint_as_float(a[j]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // every slice of the tile is in its CTA's shared memory
+
+  // ------------------------------------------------------------------ cluster reduction
+  // CTA s finishes rows [s * rr, (s + 1) * rr) of the tile for every token: consecutive
+  // threads take consecutive rows, so the writes of y[t, n0 + row] are contiguous.
+  {
+    const int rr = kSkRows / S;
+    const uint32_t part_addr = smem_u32(part);
+    for (int e = threadIdx.x; e < rr * T; e += kSkThreads) {
+      const int t = e / rr;
+      const int row = s * rr + (e - t * rr);
+      const int n = n0 + row;
+      if (n >= N) continue;
+      float acc[NMAT];
+#pragma unroll
+      for (int mat = 0; mat < NMAT; ++mat) {
+        const uint32_t off =
+            static_cast<uint32_t>(((mat * Tpad + t) * kSkRows + row) * static_cast<int>(sizeof(float)));
+        float v = 0.f;
+        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(mapa_shared(part_addr + off, static_cast<uint32_t>(q)));
+        acc[mat] = v;
+      }
+      float out;
+      if (EPI == EPI_GEGLU) {
+        out = gelu_tanh_f(acc[0]) * acc[NMAT - 1];
+      } else {
+        const float z = acc[0] + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
+        out = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
+      }
+      y[static_cast<size_t>(t) * N + n] = __float2bfloat16_rn(out);
+    }
+  }
+  cluster_sync();   // no CTA leaves while another may still read its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+// Shared memory of one CTA: the stage ring (also the slice buffer afterwards), the mbarriers
+// and the TMEM address slot, plus 1 KB for the 1024-byte alignment of the ring.
+static int skinny_smem(int nmat, int tpad, int stages) {
+  const int stage_bytes = nmat * kSkA + tpad * kSkBK * 2;
+  return 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
+}
+
+int gemm_skinny_stages(int nmat, int tpad) {
+  const int stage_bytes = nmat * kSkA + tpad * kSkBK * 2;
+  int stages = (192 * 1024) / stage_bytes;
+  if (stages > 8) stages = 8;
+  // the ring must also hold the fp32 slice [nmat][tpad][128]
+  while (stages * stage_bytes < nmat * tpad * kSkRows * 4) ++stages;
+  return skinny_smem(nmat, tpad, stages) <= 232448 ? stages : 0;
+}
+
+template <int EPI, int NMAT>
+static cudaError_t launch_skinny_t(const SkinnyLaunch& L) {
+  auto kern = gemm_skinny_kernel<EPI, NMAT>;
+  const int stages = gemm_skinny_stages(NMAT, L.tpad);
+  if (stages == 0) return cudaErrorInvalidValue;
+  const int smem = skinny_smem(NMAT, L.tpad, stages);
+  static SmemAttrCache cache;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem, cache);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.tiles * L.split, 1, 1);
+  cfg.blockDim = dim3(kSkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = L.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = L.pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tmW0, L.tmW1, L.tmX,
+                            static_cast<const __nv_bfloat16*>(L.bias),
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.N, L.K, L.tpad, stages,
+                            L.gelu_mode, L.status, L.timeout_ns);
+}
+
+cudaError_t gemm_skinny_launch(const SkinnyLaunch& L) {
+  const int num_kb = (L.K + kSkBK - 1) / kSkBK;
+  if (L.T < 1 || L.T > kSkinnyMaxT || L.tpad < L.T || L.tpad % 32 != 0 || L.tpad > kSkinnyMaxT ||
+      L.tiles < 1 || (L.split != 1 && L.split != 2 && L.split != 4 && L.split != 8) ||
+      L.split > num_kb)
+    return cudaErrorInvalidValue;
+  switch (L.epi) {
+    case EPI_BIAS: return launch_skinny_t<EPI_BIAS, 1>(L);
+    case EPI_BIAS_GELU: return launch_skinny_t<EPI_BIAS_GELU, 1>(L);
+    case EPI_GEGLU: return launch_skinny_t<EPI_GEGLU, 2>(L);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fmlp

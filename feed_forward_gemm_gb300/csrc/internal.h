@@ -57,6 +57,28 @@ struct GemmLaunch {
   uint64_t timeout_ns;
 };
 
+// Few-token tcgen05 GEMM (weights as the MMA's M side, K split over a cluster; gemm_skinny.cu).
+constexpr int kSkinnyMaxT = 128;
+struct SkinnyLaunch {
+  CUtensorMap tmW0;   // weights [N, K] bf16, box {64, 128}, 128B swizzle (Wg for GeGLU)
+  CUtensorMap tmW1;   // Wu for GeGLU (else a copy of tmW0)
+  CUtensorMap tmX;    // x [T, K] bf16, box {64, tpad}, 128B swizzle
+  const void* bias;   // [N] or nullptr
+  void* y;            // [T, N] bf16
+  int T, N, K;
+  int tpad;           // T rounded up to a multiple of 32 (the MMA's N)
+  int tiles;          // ceil(N / 128)
+  int split;          // K slices per tile = cluster size: 1, 2, 4 or 8
+  int epi, gelu_mode;
+  bool pdl;
+  cudaStream_t stream;
+  int* status;
+  uint64_t timeout_ns;
+};
+cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
+// Pipeline stages for nmat weight matrices and tpad token rows (0: does not fit).
+int gemm_skinny_stages(int nmat, int tpad);
+
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
 // CTA-pair (cta_group::2) kernel: 256 x 256 tiles over clusters of two CTAs; bn is 256;
 // grid = 2 x pairs.

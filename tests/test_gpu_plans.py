@@ -80,12 +80,32 @@ def test_fused_small_workload_and_determinism():
     assert_parity(a, oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"]), "geglu 1024x32x64")
 
 
-# ------------------------------------------------------------------------ GEMV plan
+# ------------------------------------------------------------------------ decode sizes
+
+SMALL_WEIGHTS = 16 << 20   # the GEMV serves two tokens when a call's weights fit in this
+
+
+def decode_plan(T, weight_bytes):
+    """The plan the decode crossover picks: the GEMV at one token, and at two when the weights
+    are small; the few-token tcgen05 kernel (a TC plan) otherwise."""
+    gemv = T == 1 or (T == 2 and weight_bytes <= SMALL_WEIGHTS)
+    return fm.FMLP_PLAN_GEMV if gemv else fm.FMLP_PLAN_TC
+
+
+def test_decode_crossover_table():
+    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(2, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_geglu_plan(3, 768, 3072) == fm.FMLP_PLAN_TC
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 4, 4096, 4096, 4096)
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 128, 4096, 4096, 4096)
+    assert "few-token" not in fm.fmlp_describe_plan("mlp", 129, 4096, 4096, 4096)
+
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4])
 @pytest.mark.parametrize("K,N", [(256, 64), (512, 1000), (4096, 4096), (3072, 768)])
 def test_gemv_linear_vs_oracle(T, K, N):
-    assert fm.fmlp_linear_plan(T, K, N) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_linear_plan(T, K, N) == decode_plan(T, N * K * 2)
     x, W, b = rbits((T, K)), ubits((N, K), 1 / math.sqrt(K)), ubits((N,), 1 / math.sqrt(K))
     _, y, check = guarded_bf16(T, N)
     fm.fmlp_linear_bias(to_dev(x), to_dev(W), to_dev(b), y, T, K, N)
@@ -96,7 +116,7 @@ def test_gemv_linear_vs_oracle(T, K, N):
 
 @pytest.mark.parametrize("T,D,H", [(1, 256, 512), (2, 768, 3072), (4, 512, 1280)])
 def test_gemv_geglu_vs_oracle(T, D, H):
-    assert fm.fmlp_geglu_plan(T, D, H) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_geglu_plan(T, D, H) == decode_plan(T, 3 * D * H * 2)
     x, Wg, Wu, Wd = geglu_inputs(T, D, H)
     assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"gemv geglu {T}x{D}x{H}")
     # the gate/up stage on its own
@@ -234,7 +254,8 @@ def test_decode_weights_written_by_previous_kernels():
     yB = empty_bf16(1, DoB)
     wsA = workspace(fm.fmlp_mlp_gelu_workspace_size(TA, DA, HA, DoA))
     wsB = workspace(fm.fmlp_mlp_gelu_workspace_size(1, DB, HB, DoB))
-    assert fm.fmlp_mlp_gelu_plan(TA, DA, HA, DoA) == fm.FMLP_PLAN_GEMV
+    # block A runs the few-token tcgen05 kernels, block B the GEMVs
+    assert fm.fmlp_mlp_gelu_plan(TA, DA, HA, DoA) == fm.FMLP_PLAN_TC
     assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == fm.FMLP_PLAN_GEMV
     torch.cuda.synchronize()
     with torch.cuda.stream(s):

@@ -432,6 +432,24 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
                    "timing": "CUDA graph of 20 consecutive forwards over 5 rotating weight sets "
                              "(336 MB > 2x L2), replayed 20 times; us_stream_launched: the same "
                              "calls launched from Python one by one"}
+    # the same MLP at 16 and 64 tokens (the few-token tcgen05 kernel), same rotation
+    for T in (16, 64):
+        xT = torch.cat([s["x"] for s in sets] * ((T + 4) // 5))[:T].contiguous()
+        yT = torch.empty((T, w.Dout), dtype=torch.bfloat16, device=dev)
+        wsbT = fm.fmlp_mlp_gelu_workspace_size(T, w.D, w.H, w.Dout)
+        wsT = torch.empty(max(wsbT, 1), dtype=torch.uint8, device=dev)
+
+        def twentyT(st, T=T, xT=xT, yT=yT, wsT=wsT, wsbT=wsbT):
+            for i in range(20):
+                s = sets[i % 5]
+                fm.fmlp_mlp_gelu(xT, s["W1"], s["b1"], s["W2"], s["b2"], yT, T, w.D, w.H, w.Dout,
+                                 fm.FMLP_GELU_ERF, wsT, wsbT, st)
+        ms_T = graph_time(torch, dev, twentyT, 20) / 20
+        gbs_T = wbytes / (ms_T * 1e-3) / 1e9
+        out[f"mlp_4096_t{T}"] = {"us": round(ms_T * 1e3, 2), "weight_GBps": round(gbs_T, 1),
+                                 "frac_hbm": round(gbs_T / pk["hbm_gbs"], 4),
+                                 "plan": fm.fmlp_mlp_gelu_plan(T, w.D, w.H, w.Dout),
+                                 "timing": "as mlp_4096_t1, with T tokens"}
     sets.clear()
     del y, ws
 

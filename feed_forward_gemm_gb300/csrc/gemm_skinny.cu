@@ -1,4 +1,4 @@
-// tcgen05 GEMM for few tokens (5..128): y[T, N] = epi(x[T, K] W[N, K]^T), weights as the M side.
+// tcgen05 GEMM for few tokens (2..128): y[T, N] = epi(x[T, K] W[N, K]^T), weights as the M side.
 //
 // With T <= 128 the usual tiling (128 token rows per tile) leaves most of the MMA's M rows
 // padding and, worse, has only N / BN tiles to spread over the SMs, so a few dozen SMs stream

@@ -1,4 +1,7 @@
-// Weight-streaming GEMV for a few tokens (decode): y[t, n] = epi(sum_k x[t, k] W[n, k] (+ b[n])).
+// Weight-streaming GEMV for one to four tokens (decode):
+//   y[t, n] = epi(sum_k x[t, k] W[n, k] (+ b[n])).
+// The host uses it for one token, and for two when the call's weights are small; the
+// few-token tcgen05 kernel (gemm_skinny.cu) is faster from there on.
 //
 // At one token the feed-forward block reads every weight once and does one multiply-add per
 // weight, so it is bound by HBM bandwidth and by launch latency (ainews.cool fused-MLP

@@ -87,7 +87,7 @@ cudaError_t gemm_tc2_max_pairs(int* pairs);
 // Dynamic shared memory a GEMM configuration needs (0 if the configuration does not exist).
 int gemm_tc_smem_bytes(int epi, int bn);
 
-// Weight-streaming GEMV for T <= kGemvMaxT tokens (decode).
+// Weight-streaming GEMV for T <= kGemvMaxT tokens (decode; the plans use it for one or two).
 constexpr int kGemvMaxT = 4;
 // Shared memory holds x and the per-segment partial sums.
 constexpr size_t kGemvMaxSmem = 200 * 1024;

@@ -85,9 +85,12 @@ typedef enum { FMLP_GELU_TANH = 0, FMLP_GELU_ERF = 1, FMLP_RELU = 2 } fmlp_gelu_
 /* Which kernel sequence a call with these sizes runs (reported by the *_plan queries). */
 typedef enum {
     FMLP_PLAN_NONE = 0,         /* T == 0: nothing launched */
-    FMLP_PLAN_TC = 1,           /* tcgen05 GEMM kernel(s); GeGLU/MLP: 2 kernels, m/h in ws */
+    FMLP_PLAN_TC = 1,           /* tcgen05 GEMM kernel(s) (the few-token kernel for 2..128
+                                   tokens, the batched ones above); GeGLU/MLP: 2 kernels,
+                                   m/h in ws */
     FMLP_PLAN_FUSED_SMALL = 2,  /* GeGLU: whole block in 1 kernel, m kept on chip */
-    FMLP_PLAN_GEMV = 3          /* few tokens: weight-streaming GEMV kernel(s) */
+    FMLP_PLAN_GEMV = 3          /* one token (two when the call's weights are <= 16 MiB):
+                                   weight-streaming GEMV kernel(s) */
 } fmlp_plan;
 
 /* y[T, out] = bf16(x[T, in] @ W[out, in]^T + b[out]).

@@ -18,7 +18,8 @@ from . import _build
 
 __all__ = [
     "FmlpError", "load", "build", "library_path",
-    "fmlp_linear_bias", "fmlp_linear_bias_gelu", "fmlp_geglu_gate_up", "fmlp_geglu",
+    "fmlp_linear_bias", "fmlp_linear_bias_strided", "fmlp_linear_bias_gelu",
+    "fmlp_geglu_gate_up", "fmlp_geglu",
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
     "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
@@ -47,6 +48,7 @@ _INT = ctypes.c_int
 # name -> (restype, argtypes); the order matches include/fmlp.h
 _SIGNATURES = {
     "fmlp_linear_bias": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fmlp_linear_bias_strided": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "fmlp_linear_bias_gelu": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P]),
     "fmlp_geglu_gate_up": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fmlp_geglu": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -156,6 +158,25 @@ def fmlp_linear_bias(x, W, b, y, T, in_dim, out_dim, stream=None, raise_on_error
     st = load().fmlp_linear_bias(_ptr(x), _ptr(W), _ptr(b), _ptr(y), T, in_dim, out_dim,
                                  _stream(stream))
     return _check(st, "fmlp_linear_bias", raise_on_error)
+
+
+def _view(t, ld):
+    """(device pointer, row stride in elements) of a row-major view whose rows may be apart."""
+    if t is None or isinstance(t, int):
+        return t, (0 if ld is None else int(ld))
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("fmlp strided views must be 2-D with unit column stride")
+    return (t.data_ptr() or None), (t.stride(0) if ld is None else int(ld))
+
+
+def fmlp_linear_bias_strided(x, W, b, y, T, in_dim, out_dim, ldx=None, ldy=None, stream=None,
+                             raise_on_error=True):
+    """fmlp_linear_bias on row-strided views; ldx/ldy default to the views' row strides."""
+    px, lx = _view(x, ldx)
+    py, ly = _view(y, ldy)
+    st = load().fmlp_linear_bias_strided(px, lx, _ptr(W), _ptr(b), py, ly, T, in_dim, out_dim,
+                                         _stream(stream))
+    return _check(st, "fmlp_linear_bias_strided", raise_on_error)
 
 
 def fmlp_linear_bias_gelu(x, W, b, h, T, in_dim, out_dim, mode=FMLP_GELU_TANH, stream=None,

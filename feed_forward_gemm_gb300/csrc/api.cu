@@ -120,10 +120,11 @@ fmlp_status device_state(DeviceState** out) {
 }
 
 // Row-major bf16 matrix [rows, cols] -> 2-D tensor map with a {64, box_rows} box, 128B swizzle.
+// ld: row stride in elements (0: rows are packed, ld = cols).
 fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
-                     uint32_t box_rows, const char* name) {
+                     uint32_t box_rows, const char* name, int64_t ld = 0) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2u};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld > 0 ? ld : cols) * 2u};
   cuuint32_t box[2] = {64u, box_rows};
   cuuint32_t es[2] = {1u, 1u};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
@@ -141,16 +142,36 @@ fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
 
 // ------------------------------------------------------------------------- validation
 
+// A region of device memory: `rows` rows of `bytes` bytes, `ld` bytes apart (rows == 1: one
+// contiguous run of `bytes`).
 struct Range {
   const void* p;
   size_t bytes;
   const char* name;
+  int64_t rows = 1;
+  size_t ld = 0;
 };
+
+size_t span(const Range& r) { return r.rows > 1 ? (r.rows - 1) * r.ld + r.bytes : r.bytes; }
+
+int64_t floor_div(int64_t a, int64_t b) { return a / b - ((a % b != 0) && ((a < 0) != (b < 0))); }
 
 bool overlaps(const Range& a, const Range& b) {
   if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
-  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+  if (!(a0 < b0 + span(b) && b0 < a0 + span(a))) return false;
+  // Two row-strided regions with the same stride (views of one buffer, such as two column
+  // blocks): row i of a is [a0 + i ld, + wa) and row j of b is [b0 + j ld, + wb); they meet
+  // iff some k = j - i in [-(rows_a - 1), rows_b - 1] has -wb < (b0 - a0) + k ld < wa.
+  if (a.rows > 1 && b.rows > 1 && a.ld == b.ld && a.bytes <= a.ld && b.bytes <= b.ld) {
+    const int64_t ld = static_cast<int64_t>(a.ld);
+    const int64_t d = static_cast<int64_t>(b0) - static_cast<int64_t>(a0);
+    const int64_t wa = static_cast<int64_t>(a.bytes), wb = static_cast<int64_t>(b.bytes);
+    const int64_t klo = std::max<int64_t>(floor_div(-wb - d, ld) + 1, -(a.rows - 1));
+    const int64_t khi = std::min<int64_t>(-floor_div(-(wa - d), ld) - 1, b.rows - 1);
+    return klo <= khi;
+  }
+  return true;   // spans meet: treat as overlapping
 }
 
 fmlp_status check_T(int64_t T) {
@@ -298,7 +319,8 @@ int skinny_split(const DeviceState& d, int64_t N_out, int64_t K) {
 
 fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const void* B0,
                           const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
-                          int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
+                          int64_t K, int gelu_mode, bool pdl, cudaStream_t s, int64_t lda,
+                          int64_t ldy) {
   SkinnyLaunch L;
   memset(&L, 0, sizeof L);
   L.tpad = static_cast<int>((M + 31) / 32 * 32);
@@ -308,12 +330,13 @@ fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const vo
   } else {
     L.tmW1 = L.tmW0;
   }
-  FMLP_TRY(make_map(&L.tmX, A, M, K, static_cast<uint32_t>(L.tpad), "x"));
+  FMLP_TRY(make_map(&L.tmX, A, M, K, static_cast<uint32_t>(L.tpad), "x", lda));
   L.bias = bias;
   L.y = Y;
   L.T = static_cast<int>(M);
   L.N = static_cast<int>(N_out);
   L.K = static_cast<int>(K);
+  L.ldy = static_cast<int>(ldy > 0 ? ldy : N_out);
   L.tiles = static_cast<int>((N_out + 127) / 128);
   L.split = skinny_split(d, N_out, K);
   L.epi = epi;
@@ -327,10 +350,13 @@ fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const vo
   return FMLP_OK;
 }
 
+// lda, ldy: row strides of A and Y in elements (0: packed rows).
 fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void* B0,
                         const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
-                        int64_t K, int gelu_mode, bool pdl, cudaStream_t s) {
-  if (use_skinny(M)) return launch_skinny(d, epi, A, B0, B1, bias, Y, M, N_out, K, gelu_mode, pdl, s);
+                        int64_t K, int gelu_mode, bool pdl, cudaStream_t s, int64_t lda = 0,
+                        int64_t ldy = 0) {
+  if (use_skinny(M))
+    return launch_skinny(d, epi, A, B0, B1, bias, Y, M, N_out, K, gelu_mode, pdl, s, lda, ldy);
   GemmLaunch L;
   memset(&L, 0, sizeof L);
   const bool geglu = epi == EPI_GEGLU;
@@ -338,14 +364,14 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   const bool pair = ch.pair;
   L.bn = ch.bn;
   const uint32_t b_rows = static_cast<uint32_t>(pair || geglu ? L.bn / 2 : L.bn);
-  FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A"));
+  FMLP_TRY(make_map(&L.tmA, A, M, K, 128, "A", lda));
   FMLP_TRY(make_map(&L.tmB0, B0, N_out, K, b_rows, "B"));
   if (geglu) {
     FMLP_TRY(make_map(&L.tmB1, B1, N_out, K, b_rows, "B_up"));
   } else {
     L.tmB1 = L.tmB0;
   }
-  FMLP_TRY(make_map(&L.tmY, Y, M, N_out, 32, "Y"));
+  FMLP_TRY(make_map(&L.tmY, Y, M, N_out, 32, "Y", ldy));
   L.bias = bias;
   L.M = static_cast<int>(M);
   L.N_out = static_cast<int>(N_out);
@@ -414,9 +440,11 @@ int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
   return FMLP_PLAN_TC;
 }
 
+// ldx, ldy: row strides of x and y in elements (0: packed rows).
 fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void* W0,
                         const void* W1, const void* bias, void* y, int64_t T, int64_t K,
-                        int64_t N, int gelu_mode, cudaStream_t s) {
+                        int64_t N, int gelu_mode, cudaStream_t s, int64_t ldx = 0,
+                        int64_t ldy = 0) {
   GemvLaunch L;
   L.x = x;
   L.W0 = W0;
@@ -428,6 +456,8 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
   L.N = static_cast<int>(N);
   L.epi = epi;
   L.gelu_mode = gelu_mode;
+  L.ldx = static_cast<int>(ldx > 0 ? ldx : K);
+  L.ldy = static_cast<int>(ldy > 0 ? ldy : N);
   L.grid = gemv_grid(static_cast<int>(T), static_cast<int>(K), static_cast<int>(N),
                      epi == EPI_GEGLU ? 2 : 1, d.sms);
   L.stream = s;
@@ -513,13 +543,27 @@ int fmlp_linear_plan(int64_t T, int64_t in, int64_t out) {
   return plan_linear(T, in, out, kPlanSms);
 }
 
+// ldx, ldy: row strides of x and y in elements (0: packed rows).
 static fmlp_status linear_common(const void* x, const void* W, const void* b, void* y,
                                  int64_t T, int64_t in, int64_t out, int epi, int mode,
-                                 fmlp_stream_t s) {
+                                 fmlp_stream_t s, int64_t ldx = 0, int64_t ldy = 0) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
   FMLP_TRY(check_inner(in, "in"));
   FMLP_TRY(check_inner(out, "out"));
+  if (ldx == 0) ldx = in;
+  if (ldy == 0) ldy = out;
+  if (ldx < in || ldy < out || ldx > kMaxDim || ldy > kMaxDim) {
+    set_error("row strides ldx = %lld, ldy = %lld must be at least in = %lld, out = %lld",
+              static_cast<long long>(ldx), static_cast<long long>(ldy),
+              static_cast<long long>(in), static_cast<long long>(out));
+    return FMLP_ERR_SHAPE;
+  }
+  if (ldx % 8 != 0 || ldy % 8 != 0) {
+    set_error("row strides ldx = %lld, ldy = %lld are not multiples of 8 elements (16 bytes)",
+              static_cast<long long>(ldx), static_cast<long long>(ldy));
+    return FMLP_ERR_ALIGN;
+  }
   if (epi == EPI_BIAS_GELU && !act_mode_ok(mode)) {
     set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU", mode);
     return FMLP_ERR_SHAPE;
@@ -528,8 +572,9 @@ static fmlp_status linear_common(const void* x, const void* W, const void* b, vo
   FMLP_NONNULL(x, "x");
   FMLP_NONNULL(W, "W");
   FMLP_NONNULL(y, "y");
-  const Range rx{x, mat_bytes(T, in), "x"}, rw{W, mat_bytes(out, in), "W"},
-      rb{b, b ? mat_bytes(1, out) : 0, "b"}, ry{y, mat_bytes(T, out), "y"};
+  const Range rx{x, mat_bytes(1, in), "x", T, mat_bytes(1, ldx)},
+      rw{W, mat_bytes(out, in), "W"}, rb{b, b ? mat_bytes(1, out) : 0, "b"},
+      ry{y, mat_bytes(1, out), "y", T, mat_bytes(1, ldy)};
   const Range ins[3] = {rx, rw, rb};
   const Range all[4] = {rx, rw, rb, ry};
   FMLP_TRY(check_ptrs(all, 4));
@@ -538,13 +583,19 @@ static fmlp_status linear_common(const void* x, const void* W, const void* b, vo
   FMLP_TRY(device_state(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   if (plan_linear(T, in, out, d->sms) == FMLP_PLAN_GEMV)
-    return launch_gemv(*d, epi, x, W, nullptr, b, y, T, in, out, mode, st);
-  return launch_gemm(*d, epi, x, W, nullptr, b, y, T, out, in, mode, false, st);
+    return launch_gemv(*d, epi, x, W, nullptr, b, y, T, in, out, mode, st, ldx, ldy);
+  return launch_gemm(*d, epi, x, W, nullptr, b, y, T, out, in, mode, false, st, ldx, ldy);
 }
 
 fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y, int64_t T,
                              int64_t in, int64_t out, fmlp_stream_t s) {
   return linear_common(x, W, b, y, T, in, out, EPI_BIAS, 0, s);
+}
+
+fmlp_status fmlp_linear_bias_strided(const void* x, int64_t ldx, const void* W, const void* b,
+                                     void* y, int64_t ldy, int64_t T, int64_t in, int64_t out,
+                                     fmlp_stream_t s) {
+  return linear_common(x, W, b, y, T, in, out, EPI_BIAS, 0, s, ldx, ldy);
 }
 
 fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,

@@ -51,8 +51,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                        const __grid_constant__ CUtensorMap tmW1,
                        const __grid_constant__ CUtensorMap tmX,
                        const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ y,
-                       int T, int N, int K, int Tpad, int stages, int gelu_mode, int* status,
-                       uint64_t timeout_ns) {
+                       int T, int N, int K, int ldy, int Tpad, int stages, int gelu_mode,
+                       int* status, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int b_bytes = Tpad * kSkBK * 2;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const float z = acc[0] + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
         out = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
       }
-      y[static_cast<size_t>(t) * N + n] = __float2bfloat16_rn(out);
+      y[static_cast<size_t>(t) * ldy + n] = __float2bfloat16_rn(out);
     }
   }
   cluster_sync();   // no CTA leaves while another may still read its shared memory
@@ -248,7 +248,7 @@ static cudaError_t launch_skinny_t(const SkinnyLaunch& L) {
   cfg.numAttrs = L.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, L.tmW0, L.tmW1, L.tmX,
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.N, L.K, L.tpad, stages,
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.N, L.K, L.ldy, L.tpad, stages,
                             L.gelu_mode, L.status, L.timeout_ns);
 }
 

@@ -92,7 +92,7 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
                                           const __nv_bfloat16* __restrict__ W1,
                                           const __nv_bfloat16* __restrict__ bias,
                                           __nv_bfloat16* __restrict__ y, int T, int K, int N,
-                                          int gelu_mode, int r0, int r1) {
+                                          int ldx, int ldy, int gelu_mode, int r0, int r1) {
   const int rows = r1 - r0;
   const int segs = K / kSeg;
   const int per_mat = rows * segs;
@@ -123,9 +123,12 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   };
   load_batch(g0);   // in flight while x is staged
 
-  const int xvec = T * (K / 8);
-  for (int i = threadIdx.x; i < xvec; i += kGemvThreads)
-    xs[i] = ld_cg_v4(reinterpret_cast<const uint4*>(x) + i);
+  // x rows are ldx elements apart (a multiple of 8); xs packs them
+  const int kvec = K / 8, xvec = T * kvec;
+  for (int i = threadIdx.x; i < xvec; i += kGemvThreads) {
+    const int t = i / kvec;
+    xs[i] = ld_cg_v4(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * ldx) + (i - t * kvec));
+  }
   __syncthreads();
 
   float acc[TMAX];
@@ -177,7 +180,7 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
       const float z = s0 + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
       v = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
     }
-    y[static_cast<size_t>(t) * N + n] = __float2bfloat16_rn(v);
+    y[static_cast<size_t>(t) * ldy + n] = __float2bfloat16_rn(v);
   }
   __syncthreads();   // the shared memory may be reused by the caller
 }
@@ -190,12 +193,13 @@ template <int EPI, int NMAT, int TMAX>
 __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
                 const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ y, int T, int K, int N, int gelu_mode) {
+                __nv_bfloat16* __restrict__ y, int T, int K, int N, int ldx, int ldy,
+                int gelu_mode) {
   extern __shared__ __align__(16) uint8_t gsm[];
   const int r0 = split_row(blockIdx.x, N), r1 = split_row(blockIdx.x + 1, N);
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait_primary();
-  gemv_rows<EPI, NMAT, TMAX>(gsm, x, W0, W1, bias, y, T, K, N, gelu_mode, r0, r1);
+  gemv_rows<EPI, NMAT, TMAX>(gsm, x, W0, W1, bias, y, T, K, N, ldx, ldy, gelu_mode, r0, r1);
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
@@ -234,7 +238,8 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
                             static_cast<const __nv_bfloat16*>(L.W0),
                             static_cast<const __nv_bfloat16*>(L.W1),
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.gelu_mode);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.K, L.N, L.ldx, L.ldy,
+                            L.gelu_mode);
 }
 
 cudaError_t gemv_launch(const GemvLaunch& L) {

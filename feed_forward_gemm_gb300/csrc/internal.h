@@ -66,6 +66,7 @@ struct SkinnyLaunch {
   const void* bias;   // [N] or nullptr
   void* y;            // [T, N] bf16
   int T, N, K;
+  int ldy;            // row stride of y in elements
   int tpad;           // T rounded up to a multiple of 32 (the MMA's N)
   int tiles;          // ceil(N / 128)
   int split;          // K slices per tile = cluster size: 1, 2, 4 or 8
@@ -98,6 +99,7 @@ struct GemvLaunch {
   const void* bias;   // [N] or nullptr
   void* y;            // [T, N]
   int T, K, N;
+  int ldx, ldy;       // row strides of x and y in elements
   int epi;
   int gelu_mode;
   int grid;

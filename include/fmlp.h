@@ -99,6 +99,18 @@ typedef enum {
 FMLP_API fmlp_status fmlp_linear_bias(const void* x, const void* W, const void* b, void* y,
                              int64_t T, int64_t in, int64_t out, fmlp_stream_t s);
 
+/* fmlp_linear_bias on row-strided views: row t of x starts at x + t * ldx and row t of y at
+ * y + t * ldy (in elements), as with a slice x[:, a:a+in] of a wider tensor (section "What's
+ * the transpose doing?": strides describe a view without moving data). ldx >= in and ldy >= out
+ * (else FMLP_ERR_SHAPE), both multiples of 8 (the 16-byte TMA row rule; else FMLP_ERR_ALIGN);
+ * 0 means packed rows. y must not share an element with x, W or b; two views of one buffer
+ * with the same stride are compared element-exactly (column blocks that interleave row by
+ * row do not overlap), other pairs by the bytes they span. W and b stay packed. Same kernels
+ * and plans as fmlp_linear_bias. */
+FMLP_API fmlp_status fmlp_linear_bias_strided(const void* x, int64_t ldx, const void* W,
+                                              const void* b, void* y, int64_t ldy, int64_t T,
+                                              int64_t in, int64_t out, fmlp_stream_t s);
+
 /* h[T, out] = bf16(act(x[T, in] @ W[out, in]^T + b[out])), act = GELU or ReLU per `mode`, b
  * nullable. The first half of fmlp_mlp_gelu as its own call (bias+activation epilogue). */
 FMLP_API fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,

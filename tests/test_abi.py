@@ -154,3 +154,32 @@ def test_tile_policy_validation(lib):
     assert fm.fmlp_set_tile_policy(7, raise_on_error=False) == fm.FMLP_ERR_SHAPE
     for p in (fm.FMLP_TILES_SINGLE, fm.FMLP_TILES_PAIR, fm.FMLP_TILES_AUTO):
         assert fm.fmlp_set_tile_policy(p) == fm.FMLP_OK
+
+
+def test_linear_strided_validation_and_view_overlap(lib):
+    """Row-strided views: stride rules, and the overlap rule for views of one buffer (exact
+    for equal strides, by byte span otherwise). Calls that pass validation stop at the missing
+    device here, never at FMLP_ERR_ALIAS."""
+    def call(x=A, ldx=1024, y=A + GB, ldy=1024, T=16, i=256, o=512, W=A + 2 * GB, b=None):
+        return fm.fmlp_linear_bias_strided(x, W, b, y, T, i, o, ldx=ldx, ldy=ldy, stream=0,
+                                           raise_on_error=False)
+    assert call(ldx=128) == fm.FMLP_ERR_SHAPE              # ldx < in
+    assert call(ldy=256) == fm.FMLP_ERR_SHAPE              # ldy < out
+    assert call(ldx=260) == fm.FMLP_ERR_ALIGN              # not a multiple of 8 elements
+    assert call(ldy=1028) == fm.FMLP_ERR_ALIGN
+    assert call(T=0, x=0, y=0) == fm.FMLP_OK
+    # x = buf[:, 0:256], y = buf[:, 256:768] of one [16, 1024] bf16 buffer: disjoint columns
+    assert call(x=A, y=A + 256 * 2) not in (fm.FMLP_ERR_ALIAS, fm.FMLP_OK)
+    # y = buf[:, 248:760] shares columns 248..255 with x on every row
+    assert call(x=A, y=A + 248 * 2) == fm.FMLP_ERR_ALIAS
+    assert "overlaps" in fm.fmlp_last_error()
+    # y = buf[:, 768:1024] (out = 256) and x = buf[:, 0:256]: disjoint; y starting one row down
+    # at columns 0.. of row 1 meets x's row 1
+    assert call(x=A, y=A + 768 * 2, o=256) not in (fm.FMLP_ERR_ALIAS, fm.FMLP_OK)
+    assert call(x=A, y=A + 1024 * 2, o=256) == fm.FMLP_ERR_ALIAS
+    # y entirely below x's last row: no overlap
+    assert call(x=A, y=A + 16 * 1024 * 2, o=256) not in (fm.FMLP_ERR_ALIAS, fm.FMLP_OK)
+    # different strides whose byte spans meet are treated as overlapping
+    assert call(x=A, y=A + 256 * 2, ldy=2048) == fm.FMLP_ERR_ALIAS
+    # y may not overlap the packed weight either
+    assert call(y=A + 2 * GB + 64) == fm.FMLP_ERR_ALIAS

@@ -6,7 +6,8 @@ fmlp_oracle.c (plain loops, double precision, bf16 rounding only where the fused
 rounds); this wrapper only marshals numpy arrays of bf16 bit patterns.
 
 Parity pins (tests/test_oracle.py): GELU against the normal CDF table and torch's fp64
-GELU, ReLU against torch's relu, the page's nn.Linear layout worked example, identity/zero weights, special cases with
+GELU, ReLU against torch's relu, the MoE block against torch per expert and against the plain
+block when every expert holds the same weights, the page's nn.Linear layout worked example, identity/zero weights, special cases with
 distinguishable operands, rounding against an independent exact rounding, and brute force
 against torch's fp64 nn.Linear / F.gelu on tiny shapes. No function here is unpinned.
 """
@@ -107,6 +108,29 @@ def gelu(x: np.ndarray, mode: int = GELU_TANH) -> np.ndarray:
     _load().oracle_gelu(_ptr(x), _ptr(out), x.size, mode)
     return out
 
+
+
+def moe_geglu(x, offsets, Wg, Wu, Wd, want_m=False, nthreads=None):
+    """Mixture-of-experts feed-forward (the ainews.cool article's MoE note: every expert is an
+    MLP): tokens arrive grouped by expert, rows [offsets[e], offsets[e+1]) of x go through
+    expert e's GeGLU block with Wg[e], Wu[e] [H, D] and Wd[e] [D, H]. Each expert's rows are
+    exactly geglu() on those rows; nothing else is computed."""
+    x = _u16(x)
+    T, D = x.shape
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = offsets.size - 1
+    if E < 1 or offsets[0] != 0 or offsets[-1] != T or np.any(np.diff(offsets) < 0):
+        raise ValueError("offsets must rise from 0 to T")
+    H = Wg.shape[1]
+    y = np.empty((T, D), dtype=np.uint16)
+    m = np.empty((T, H), dtype=np.uint16)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b == a:
+            continue
+        ye, me = geglu(x[a:b], Wg[e], Wu[e], Wd[e], want_m=True, nthreads=nthreads)
+        y[a:b], m[a:b] = ye, me
+    return (y, m) if want_m else y
 
 def linear(x, W, b, rows=None, nthreads=None, want_acc=False):
     """y = bf16(x W^T + b) for the selected rows; returns bf16 bits (and fp64 pre-round)."""

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import (bits_to_f64, f64_to_bits_via_torch, parity_stats, rne_bf16_array,
+from helpers import (bits_to_f64, f64_to_bits_via_torch, parity_stats, rne_bf16_array, t64,
                      rne_bf16_bits, torch_geglu_f64, torch_mlp_f64)
 import synth
 
@@ -237,3 +237,43 @@ def test_mlp_identity_weights():
     # bias-free and zero first layer: y = b2
     y0 = oracle.mlp_gelu(x, np.zeros((D, D), np.uint16), None, eye, b2)
     assert np.array_equal(y0, np.broadcast_to(b2, y0.shape))
+
+
+# ---------------------------------------------------------------------------- MoE
+
+def test_moe_geglu_brute_force_vs_torch_per_expert():
+    T, D, H, E = 41, 16, 24, 4
+    offsets = [0, 9, 9, 30, 41]                 # expert 1 gets no token
+    x = rand_bits((T, D))
+    Wg, Wu = rand_bits((E, H, D), 0.3), rand_bits((E, H, D), 0.3)
+    Wd = rand_bits((E, D, H), 0.3)
+    y, m = oracle.moe_geglu(x, offsets, Wg, Wu, Wd, want_m=True)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        xf = t64(x[a:b])
+        g = torch.nn.functional.linear(xf, t64(Wg[e]))
+        u = torch.nn.functional.linear(xf, t64(Wu[e]))
+        me = rne_bf16_array((torch.nn.functional.gelu(g, approximate="tanh") * u).numpy())
+        ye = torch.nn.functional.linear(torch.from_numpy(bits_to_f64(me)), t64(Wd[e])).numpy()
+        assert np.array_equal(m[a:b], me)
+        assert np.array_equal(y[a:b], rne_bf16_array(ye))
+
+
+def test_moe_with_identical_experts_is_the_plain_block():
+    T, D, H, E = 50, 32, 40, 3
+    x = rand_bits((T, D))
+    Wg, Wu, Wd = rand_bits((H, D), 0.2), rand_bits((H, D), 0.2), rand_bits((D, H), 0.2)
+    stack = lambda w: np.stack([w] * E)
+    y = oracle.moe_geglu(x, [0, 7, 33, 50], stack(Wg), stack(Wu), stack(Wd))
+    assert np.array_equal(y, oracle.geglu(x, Wg, Wu, Wd))
+
+
+def test_moe_rejects_bad_offsets():
+    x = rand_bits((8, 16))
+    W = rand_bits((2, 8, 16), 0.1)
+    Wd = rand_bits((2, 16, 8), 0.1)
+    for bad in ([0, 9, 8], [1, 4, 8], [0, 5, 3, 8][:3]):
+        with pytest.raises(ValueError):
+            oracle.moe_geglu(x, bad, W, W, Wd)

@@ -402,6 +402,34 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
                      "l2": "flushed before every call (median of 30)"}
     del d, y, ws
 
+    # mixture of experts: 8 GeGLU experts (D 4096, H 14336, Mixtral-shaped), 16384 routed token
+    # rows in uneven groups, both GEMM stages one launch each over all experts
+    E, Dm, Hm = 8, 4096, 14336
+    counts = [4096, 3072, 2560, 2048, 1536, 1280, 1024, 768]
+    Tm = sum(counts)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5000)
+    xm = (torch.randn((Tm, Dm), generator=gen, device=dev)).to(torch.bfloat16)
+    Wgm = (torch.rand((E, Hm, Dm), generator=gen, device=dev) * 2 - 1).mul_(Dm ** -0.5).to(torch.bfloat16)
+    Wum = (torch.rand((E, Hm, Dm), generator=gen, device=dev) * 2 - 1).mul_(Dm ** -0.5).to(torch.bfloat16)
+    Wdm = (torch.rand((E, Dm, Hm), generator=gen, device=dev) * 2 - 1).mul_(Hm ** -0.5).to(torch.bfloat16)
+    offm = torch.tensor([0] + list(np.cumsum(counts)), dtype=torch.int32, device=dev)
+    ym = torch.empty((Tm, Dm), dtype=torch.bfloat16, device=dev)
+    wsm = torch.empty(fm.fmlp_moe_geglu_workspace_size(Tm, Dm, Hm), dtype=torch.uint8, device=dev)
+
+    def moe():
+        fm.fmlp_moe_geglu(xm, offm, Wgm, Wum, Wdm, ym, Tm, Dm, Hm, E, wsm, wsm.numel(), stream)
+    for _ in range(3):
+        moe()
+    ms = events_time(moe, 10)
+    fl = 2.0 * 3 * Tm * Dm * Hm
+    out["moe_geglu_8x4096x14336"] = {
+        "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+        "frac_bf16_burst": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+        "tokens_per_expert": counts, "kernel": "grouped single-SM tcgen05, one launch per stage",
+        "l2": "inputs larger than L2 (2.8 GB of expert weights)"}
+    del xm, Wgm, Wum, Wdm, offm, ym, wsm
+
     # the same MLP at one token (decode): weights rotate through 5 copies (336 MB > 2x L2)
     w = synth.WORKLOADS["mlp_4096_t1"]
     sets = []

@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "FmlpError", "load", "build", "library_path",
     "fmlp_linear_bias", "fmlp_linear_bias_strided", "fmlp_linear_bias_gelu",
-    "fmlp_geglu_gate_up", "fmlp_geglu",
+    "fmlp_geglu_gate_up", "fmlp_geglu", "fmlp_moe_geglu", "fmlp_moe_geglu_workspace_size",
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
     "fmlp_device_status", "fmlp_test_wait_timeout", "fmlp_status_string", "fmlp_last_error",
@@ -49,6 +49,9 @@ _INT = ctypes.c_int
 _SIGNATURES = {
     "fmlp_linear_bias": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fmlp_linear_bias_strided": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "fmlp_moe_geglu": (_INT, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_size_t,
+                              _P]),
+    "fmlp_moe_geglu_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "fmlp_linear_bias_gelu": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P]),
     "fmlp_geglu_gate_up": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fmlp_geglu": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -177,6 +180,18 @@ def fmlp_linear_bias_strided(x, W, b, y, T, in_dim, out_dim, ldx=None, ldy=None,
     st = load().fmlp_linear_bias_strided(px, lx, _ptr(W), _ptr(b), py, ly, T, in_dim, out_dim,
                                          _stream(stream))
     return _check(st, "fmlp_linear_bias_strided", raise_on_error)
+
+
+def fmlp_moe_geglu(x, offsets, Wg, Wu, Wd, y, T, D, H, E, ws=None, ws_bytes=0, stream=None,
+                   raise_on_error=True):
+    """Per-expert GeGLU over tokens grouped by expert (offsets: E + 1 int32 on the device)."""
+    st = load().fmlp_moe_geglu(_ptr(x), _ptr(offsets), E, _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(y),
+                               T, D, H, _ptr(ws), int(ws_bytes), _stream(stream))
+    return _check(st, "fmlp_moe_geglu", raise_on_error)
+
+
+def fmlp_moe_geglu_workspace_size(T, D, H) -> int:
+    return int(load().fmlp_moe_geglu_workspace_size(T, D, H))
 
 
 def fmlp_linear_bias_gelu(x, W, b, h, T, in_dim, out_dim, mode=FMLP_GELU_TANH, stream=None,

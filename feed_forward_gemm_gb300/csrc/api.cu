@@ -140,6 +140,28 @@ fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
   return FMLP_OK;
 }
 
+// A 3-D map over [depth, rows, cols] bf16 (packed), box {64, box_rows, 1}, 128-byte swizzle.
+fmlp_status make_map3(CUtensorMap* m, const void* ptr, int64_t depth, int64_t rows, int64_t cols,
+                      uint32_t box_rows, const char* name) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(depth)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2u,
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols) * 2u};
+  cuuint32_t box[3] = {64u, box_rows, 1u};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(%s [%lld x %lld x %lld]) failed with CUresult %d", name,
+              static_cast<long long>(depth), static_cast<long long>(rows),
+              static_cast<long long>(cols), static_cast<int>(r));
+    return FMLP_ERR_CUDA;
+  }
+  return FMLP_OK;
+}
+
 // ------------------------------------------------------------------------- validation
 
 // A region of device memory: `rows` rows of `bytes` bytes, `ld` bytes apart (rows == 1: one
@@ -674,6 +696,97 @@ fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void
     r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
     if (r == FMLP_OK)
       r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st);
+  }
+  if (!ws) {
+    cudaError_t e = cudaFreeAsync(m, st);
+    if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
+  }
+  return r;
+}
+
+size_t fmlp_moe_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
+  (void)D;
+  return T > 0 && H > 0 ? mat_bytes(T, H) : 0;
+}
+
+fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, const void* Wg,
+                           const void* Wu, const void* Wd, void* y, int64_t T, int64_t D,
+                           int64_t H, void* ws, size_t ws_bytes, fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(D, "D"));
+  FMLP_TRY(check_inner(H, "H"));
+  if (E < 1 || E > kMoeMaxExperts) {
+    set_error("E = %lld experts is outside [1, %d]", static_cast<long long>(E), kMoeMaxExperts);
+    return FMLP_ERR_SHAPE;
+  }
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(offsets, "offsets");
+  FMLP_NONNULL(Wg, "Wg");
+  FMLP_NONNULL(Wu, "Wu");
+  FMLP_NONNULL(Wd, "Wd");
+  FMLP_NONNULL(y, "y");
+  const size_t need = mat_bytes(T, H);
+  if (ws && ws_bytes < need) {
+    set_error("workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return FMLP_ERR_WORKSPACE;
+  }
+  if (reinterpret_cast<uintptr_t>(offsets) % 4 != 0) {
+    set_error("offsets is not 4-byte aligned");
+    return FMLP_ERR_ALIGN;
+  }
+  const size_t wbytes = static_cast<size_t>(E) * mat_bytes(H, D);
+  const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, wbytes, "Wg"}, ru{Wu, wbytes, "Wu"},
+      rd{Wd, wbytes, "Wd"}, ry{y, mat_bytes(T, D), "y"}, rw{ws, ws ? need : 0, "workspace"},
+      ro{offsets, static_cast<size_t>(E + 1) * 4u, "offsets"};
+  const Range all[6] = {rx, rg, ru, rd, ry, rw};
+  FMLP_TRY(check_ptrs(all, 6));
+  const Range ins_y[6] = {rx, rg, ru, rd, rw, ro};
+  FMLP_TRY(check_alias(ry, ins_y, 6));
+  const Range ins_w[5] = {rx, rg, ru, rd, ro};
+  FMLP_TRY(check_alias(rw, ins_w, 5));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  void* m = ws;
+  if (!m) {
+    cudaError_t e = cudaMallocAsync(&m, need, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+  }
+  fmlp_status r = FMLP_OK;
+  for (int stage = 0; stage < 2 && r == FMLP_OK; ++stage) {
+    // stage 0: m = gelu_tanh(x Wg[e]^T) * (x Wu[e]^T); stage 1: y = m Wd[e]^T
+    GemmLaunch L;
+    memset(&L, 0, sizeof L);
+    const bool gu = stage == 0;
+    const void* A = gu ? x : m;
+    const int64_t K = gu ? D : H, N = gu ? H : D;
+    if ((r = make_map(&L.tmA, A, T, K, 128, gu ? "x" : "m")) != FMLP_OK) break;
+    if (gu) {
+      if ((r = make_map3(&L.tmB0, Wg, E, H, D, 128, "Wg")) != FMLP_OK) break;
+      if ((r = make_map3(&L.tmB1, Wu, E, H, D, 128, "Wu")) != FMLP_OK) break;
+    } else {
+      if ((r = make_map3(&L.tmB0, Wd, E, D, H, 256, "Wd")) != FMLP_OK) break;
+      L.tmB1 = L.tmB0;
+    }
+    L.tmY = L.tmA;   // unused: the grouped epilogue stores directly
+    L.M = static_cast<int>(T);
+    L.N_out = static_cast<int>(N);
+    L.K = static_cast<int>(K);
+    L.epi = gu ? EPI_GEGLU : EPI_BIAS;
+    L.bn = 256;
+    L.grid = d->sms;   // persistent: the tile count is only known on the device
+    L.pdl = !gu;
+    L.stream = st;
+    L.status = d->status;
+    L.timeout_ns = kWaitTimeoutNs;
+    L.offsets = offsets;
+    L.groups = static_cast<int>(E);
+    L.ydir = gu ? m : y;
+    L.ldy = static_cast<int>(N);
+    const cudaError_t e = gemm_tc_grouped_launch(L);
+    if (e != cudaSuccess) r = cuda_fail(e, "grouped gemm launch");
   }
   if (!ws) {
     cudaError_t e = cudaFreeAsync(m, st);

@@ -109,4 +109,64 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
   }
 }
 
+// The same epilogue for a grouped GEMM whose tiles may end inside the tile (the last rows of
+// an expert's token group): each lane holds one output row and, when row_ok, stores its
+// columns [n_tile0, n_tile0 + BN_OUT) straight to yrow (16-byte stores, columns past N_out
+// skipped); rows past the group are computed but never written.
+template <int BN, int BN_OUT, int EPI>
+__device__ __forceinline__ void epilogue_rows_direct(uint32_t t_row, int lane, bool row_ok,
+                                                     __nv_bfloat16* yrow, int n_tile0, int N_out,
+                                                     const __nv_bfloat16* __restrict__ bias,
+                                                     int gelu_mode) {
+  (void)lane;
+#pragma unroll 1
+  for (int c = 0; c < BN_OUT; c += 32) {
+    uint32_t a[32];
+    tmem_ld_32x32b_x32(t_row + c, a);
+    if (EPI == EPI_GEGLU) {
+      uint32_t u[32];
+      tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])) * __uint_as_float(u[i]));
+    } else {
+      tmem_ld_wait();
+      const int nb = n_tile0 + c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (bias != nullptr && nb + q * 8 < N_out)
+          w = __ldg(reinterpret_cast<const uint4*>(bias + nb + q * 8));
+        const uint32_t wb[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = q * 8 + e * 2;
+          a[i] = __float_as_uint(__uint_as_float(a[i]) + bf16_lo(wb[e]));
+          a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
+        }
+      }
+      if (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          a[i] = __float_as_uint(gelu_f(__uint_as_float(a[i]), gelu_mode));
+      }
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int n = n_tile0 + c + q * 8;
+        if (n < N_out) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
+          v.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
+          v.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
+          v.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
+          *reinterpret_cast<uint4*>(yrow + n) = v;
+        }
+      }
+    }
+  }
+}
+
 }  // namespace fmlp

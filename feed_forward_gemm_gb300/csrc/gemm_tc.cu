@@ -27,6 +27,15 @@
 // one MMA with N = BN produces gate in accumulator columns [0, BN/2) and up in [BN/2, BN):
 // both share the A tile and the same instruction.
 // All waits are bounded; on expiry the kernel records a status code and unwinds.
+//
+// GROUPED (the mixture-of-experts block): the rows of A are grouped by expert, rows
+// [offsets[e], offsets[e+1]) belonging to expert e, whose weights are slice e of a 3-D tensor
+// [E, N, K]. One launch serves every expert: each CTA reads the offsets after the dependency
+// wait (a router kernel may have written them just before), counts each group's 128-row
+// tiles, and walks tiles ordered by (group row tile, N tile). A loads start at the group's
+// row; B loads take the expert's slice through a 3-D tensor map; the epilogue stores rows
+// directly and skips the rows past the group's end, which the 128-row tile computed
+// from the next group's tokens.
 #include "activation.cuh"
 #include "gemm_epilogue.cuh"
 #include "internal.h"
@@ -67,13 +76,26 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& tm
   tn = r / gm;
 }
 
-template <int BN, int EPI>
+// Group g of a GROUPED launch: tile t -> expert e, first row, rows in the tile, N tile.
+__device__ __forceinline__ void group_tile(int t, int num_n, const int* s_off, const int* s_mt,
+                                           int& e, int& row0, int& rows, int& tn) {
+  const int gm = t / num_n;
+  tn = t - gm * num_n;
+  e = 0;
+  while (s_mt[e + 1] <= gm) ++e;
+  row0 = s_off[e] + (gm - s_mt[e]) * kBM;
+  rows = min(kBM, s_off[e + 1] - row0);
+}
+
+template <int BN, int EPI, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmY, const __nv_bfloat16* __restrict__ bias,
-                   int M, int N_out, int K, int gelu_mode, int* status, uint64_t timeout_ns) {
+                   int M, int N_out, int K, int gelu_mode, int* status, uint64_t timeout_ns,
+                   const int* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ ydir,
+                   int ldy) {
   using C = Cfg<BN, EPI>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -119,10 +141,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait_primary();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const int num_m = (M + kBM - 1) / kBM;
+  int num_m = (M + kBM - 1) / kBM;
   const int num_n = (N_out + C::BN_OUT - 1) / C::BN_OUT;
-  const int num_tiles = num_m * num_n;
   const int num_kb = (K + kBK - 1) / kBK;
+  // GROUPED: token offsets and per-group prefix of 128-row tiles, in the (unused) staging area
+  int* s_off = reinterpret_cast<int*>(stg_all);
+  int* s_mt = s_off + (kMoeMaxExperts + 1);
+  if constexpr (GROUPED) {
+    for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = min(max(__ldcg(offsets + i), 0), M);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      s_mt[0] = 0;
+      for (int g = 0; g < E; ++g) {
+        s_off[g + 1] = max(s_off[g + 1], s_off[g]);   // a falling offset makes the group empty
+        acc += (s_off[g + 1] - s_off[g] + kBM - 1) / kBM;
+        s_mt[g + 1] = acc;
+      }
+    }
+    __syncthreads();
+    num_m = s_mt[E];
+  }
+  const int num_tiles = num_m * num_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -132,8 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued_mask = 0, last_phase_mask = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, num_m, num_n, tm, tn);
+        int tm = 0, tn, ge = 0, grow = 0, grows = 0;
+        if constexpr (GROUPED)
+          group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+        else
+          tile_coords(t, num_m, num_n, tm, tn);
+        const int a_row = GROUPED ? grow : tm * kBM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, status, SITE_PRODUCER_EMPTY, timeout_ns)) {
             ok = false;
@@ -142,8 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = stages + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sA, &tmA, &full[stage], kb * kBK, tm * kBM);
-          if (EPI == EPI_GEGLU) {
+          tma_load_2d(sA, &tmA, &full[stage], kb * kBK, a_row);
+          if constexpr (GROUPED) {
+            if (EPI == EPI_GEGLU) {
+              tma_load_3d(sB, &tmB0, &full[stage], kb * kBK, tn * (BN / 2), ge);
+              tma_load_3d(sB + (BN / 2) * 128, &tmB1, &full[stage], kb * kBK, tn * (BN / 2), ge);
+            } else {
+              tma_load_3d(sB, &tmB0, &full[stage], kb * kBK, tn * BN, ge);
+            }
+          } else if (EPI == EPI_GEGLU) {
             tma_load_2d(sB, &tmB0, &full[stage], kb * kBK, tn * (BN / 2));
             tma_load_2d(sB + (BN / 2) * 128, &tmB1, &full[stage], kb * kBK, tn * (BN / 2));
           } else {
@@ -213,8 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sb = 0;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      int tm, tn;
-      tile_coords(t, num_m, num_n, tm, tn);
+      int tm = 0, tn, ge = 0, grow = 0, grows = 0;
+      if constexpr (GROUPED)
+        group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+      else
+        tile_coords(t, num_m, num_n, tm, tn);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       // all lanes wait; the warp proceeds only if every lane saw the phase complete, so the
@@ -224,9 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      const int row0 = tm * kBM + wq * 32;
-      epilogue_cols<BN, C::BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * C::BN_OUT, M, N_out,
-                                        &tmY, bias, gelu_mode);
+      if constexpr (GROUPED) {
+        const int r = wq * 32 + lane;
+        epilogue_rows_direct<BN, C::BN_OUT, EPI>(t_row, lane, r < grows,
+                                                 ydir + static_cast<size_t>(grow + r) * ldy,
+                                                 tn * C::BN_OUT, N_out, bias, gelu_mode);
+      } else {
+        const int row0 = tm * kBM + wq * 32;
+        epilogue_cols<BN, C::BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * C::BN_OUT, M, N_out,
+                                          &tmY, bias, gelu_mode);
+      }
       // this warp is done reading the accumulator buffer
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
@@ -245,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------- host side
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool GROUPED = false>
 static cudaError_t launch_one(const GemmLaunch& L) {
   using C = Cfg<BN, EPI>;
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  auto kern = gemm_tc_kernel<BN, EPI, GROUPED>;
   static SmemAttrCache cache;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, cache);
   if (e != cudaSuccess) return e;
@@ -264,7 +325,8 @@ static cudaError_t launch_one(const GemmLaunch& L) {
   cfg.numAttrs = L.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB0, L.tmB1, L.tmY,
                             static_cast<const __nv_bfloat16*>(L.bias), L.M, L.N_out, L.K,
-                            L.gelu_mode, L.status, L.timeout_ns);
+                            L.gelu_mode, L.status, L.timeout_ns, L.offsets, L.groups,
+                            static_cast<__nv_bfloat16*>(L.ydir), L.ldy);
 }
 
 int gemm_tc_smem_bytes(int epi, int bn) {
@@ -291,6 +353,16 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L) {
     case EPI_BIAS_GELU * 1000 + 256: return launch_one<256, EPI_BIAS_GELU>(L);
     case EPI_GEGLU * 1000 + 128: return launch_one<128, EPI_GEGLU>(L);
     case EPI_GEGLU * 1000 + 256: return launch_one<256, EPI_GEGLU>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t gemm_tc_grouped_launch(const GemmLaunch& L) {
+  if (L.groups < 1 || L.groups > kMoeMaxExperts || !L.offsets || !L.ydir || L.bn != 256)
+    return cudaErrorInvalidValue;
+  switch (L.epi) {
+    case EPI_BIAS: return launch_one<256, EPI_BIAS, true>(L);
+    case EPI_GEGLU: return launch_one<256, EPI_GEGLU, true>(L);
     default: return cudaErrorInvalidValue;
   }
 }

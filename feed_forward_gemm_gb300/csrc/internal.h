@@ -55,7 +55,15 @@ struct GemmLaunch {
   cudaStream_t stream;
   int* status;        // device status word
   uint64_t timeout_ns;
+  // Grouped (mixture-of-experts) launches only: A rows grouped by expert, [groups + 1]
+  // device offsets; B maps are 3-D [groups, N, K]; the output goes to ydir (row stride ldy)
+  // with direct stores.
+  const int* offsets;
+  int groups;
+  void* ydir;
+  int ldy;
 };
+constexpr int kMoeMaxExperts = 256;
 
 // Few-token tcgen05 GEMM (weights as the MMA's M side, K split over a cluster; gemm_skinny.cu).
 constexpr int kSkinnyMaxT = 128;
@@ -81,6 +89,8 @@ cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
 int gemm_skinny_stages(int nmat, int tpad);
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
+// The single-SM kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).
+cudaError_t gemm_tc_grouped_launch(const GemmLaunch& L);
 // CTA-pair (cta_group::2) kernel: 256 x 256 tiles over clusters of two CTAs; bn is 256;
 // grid = 2 x pairs.
 cudaError_t gemm_tc2_launch(const GemmLaunch& L);

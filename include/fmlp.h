@@ -140,6 +140,23 @@ FMLP_API fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1
                           int64_t Dout, fmlp_gelu_mode mode, void* ws, size_t ws_bytes,
                           fmlp_stream_t s);
 
+/* Mixture-of-experts feed-forward: E experts, each a GeGLU block (the ainews.cool article's MoE
+ * note: every expert is an MLP, and fusing them cuts per-expert overhead). The tokens are
+ * already grouped by expert: rows [offsets[e], offsets[e+1]) of x [T, D] go through expert e,
+ *   m = bf16(gelu_tanh(x Wg[e]^T) * (x Wu[e]^T)),  y = bf16(m Wd[e]^T),
+ * with Wg, Wu [E, H, D] and Wd [E, D, H] packed. offsets: E + 1 int32 in device memory
+ * (4-byte aligned), rising from 0 to T; the kernels read them after waiting for the previous
+ * kernel on `s`, so a routing kernel may write them just before, and the host never reads
+ * them. Offsets outside [0, T] are clamped and a falling one empties that expert's group
+ * (rows no group covers are left as they were); nothing faults. 1 <= E <= 256. ws: T*H*2
+ * bytes (m), or NULL to take it from the stream-ordered allocator. Two kernels, each one
+ * launch over all experts. No routing, gather or scatter is done here. */
+FMLP_API fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E,
+                                    const void* Wg, const void* Wu, const void* Wd, void* y,
+                                    int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
+                                    fmlp_stream_t s);
+FMLP_API size_t fmlp_moe_geglu_workspace_size(int64_t T, int64_t D, int64_t H);
+
 /* fmlp_geglu for callers that cannot allocate device memory (no counterpart in the pages).
  *
  * Who needs it: code that may not call cudaMalloc or any allocating routine - a plugin in a

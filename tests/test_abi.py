@@ -183,3 +183,26 @@ def test_linear_strided_validation_and_view_overlap(lib):
     assert call(x=A, y=A + 256 * 2, ldy=2048) == fm.FMLP_ERR_ALIAS
     # y may not overlap the packed weight either
     assert call(y=A + 2 * GB + 64) == fm.FMLP_ERR_ALIAS
+
+
+def test_moe_validation(lib):
+    def call(**kw):
+        a = dict(x=A, off=A + 6 * GB, E=8, Wg=A + GB, Wu=A + 2 * GB, Wd=A + 3 * GB, y=A + 4 * GB,
+                 T=100, D=512, H=1024, ws=A + 5 * GB, ws_bytes=100 * 1024 * 2)
+        a.update(kw)
+        return fm.fmlp_moe_geglu(a["x"], a["off"], a["Wg"], a["Wu"], a["Wd"], a["y"], a["T"],
+                                 a["D"], a["H"], a["E"], a["ws"], a["ws_bytes"], stream=0,
+                                 raise_on_error=False)
+    assert call(E=0) == fm.FMLP_ERR_SHAPE
+    assert call(E=257) == fm.FMLP_ERR_SHAPE
+    assert call(D=100) == fm.FMLP_ERR_SHAPE
+    assert call(off=0) == fm.FMLP_ERR_NULL
+    assert call(off=A + 6 * GB + 2) == fm.FMLP_ERR_ALIGN
+    assert call(Wd=A + 3 * GB + 8) == fm.FMLP_ERR_ALIGN
+    assert call(ws_bytes=100) == fm.FMLP_ERR_WORKSPACE
+    assert call(y=A + 16) == fm.FMLP_ERR_ALIAS              # y on top of x
+    assert call(ws=A + 4 * GB) == fm.FMLP_ERR_ALIAS         # workspace on top of y
+    assert call(off=A + 4 * GB + 64) == fm.FMLP_ERR_ALIAS   # y on top of the offsets
+    assert call(T=0, x=0, y=0) == fm.FMLP_OK
+    assert fm.fmlp_moe_geglu_workspace_size(100, 512, 1024) == 100 * 1024 * 2
+    assert fm.fmlp_moe_geglu_workspace_size(0, 512, 1024) == 0

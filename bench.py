@@ -426,7 +426,7 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     out["moe_geglu_8x4096x14336"] = {
         "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
         "frac_bf16_burst": round(fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-        "tokens_per_expert": counts, "kernel": "grouped single-SM tcgen05, one launch per stage",
+        "tokens_per_expert": counts, "kernel": "grouped CTA-pair tcgen05, one launch per stage",
         "l2": "inputs larger than L2 (2.8 GB of expert weights)"}
     del xm, Wgm, Wum, Wdm, offm, ym, wsm
 

@@ -755,6 +755,9 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
   }
   fmlp_status r = FMLP_OK;
+  // CTA pairs (256-row tiles, each CTA loading 128 weight rows) when the device runs them
+  const bool pair = d->max_pairs >= 1 &&
+                    g_tile_policy.load(std::memory_order_relaxed) != FMLP_TILES_SINGLE;
   for (int stage = 0; stage < 2 && r == FMLP_OK; ++stage) {
     // stage 0: m = gelu_tanh(x Wg[e]^T) * (x Wu[e]^T); stage 1: y = m Wd[e]^T
     GemmLaunch L;
@@ -767,7 +770,7 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
       if ((r = make_map3(&L.tmB0, Wg, E, H, D, 128, "Wg")) != FMLP_OK) break;
       if ((r = make_map3(&L.tmB1, Wu, E, H, D, 128, "Wu")) != FMLP_OK) break;
     } else {
-      if ((r = make_map3(&L.tmB0, Wd, E, D, H, 256, "Wd")) != FMLP_OK) break;
+      if ((r = make_map3(&L.tmB0, Wd, E, D, H, pair ? 128 : 256, "Wd")) != FMLP_OK) break;
       L.tmB1 = L.tmB0;
     }
     L.tmY = L.tmA;   // unused: the grouped epilogue stores directly
@@ -776,7 +779,8 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
     L.K = static_cast<int>(K);
     L.epi = gu ? EPI_GEGLU : EPI_BIAS;
     L.bn = 256;
-    L.grid = d->sms;   // persistent: the tile count is only known on the device
+    // persistent: the tile count is only known on the device
+    L.grid = pair ? 2 * d->max_pairs : d->sms;
     L.pdl = !gu;
     L.stream = st;
     L.status = d->status;
@@ -785,7 +789,7 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
     L.groups = static_cast<int>(E);
     L.ydir = gu ? m : y;
     L.ldy = static_cast<int>(N);
-    const cudaError_t e = gemm_tc_grouped_launch(L);
+    const cudaError_t e = pair ? gemm_tc2_grouped_launch(L) : gemm_tc_grouped_launch(L);
     if (e != cudaSuccess) r = cuda_fail(e, "grouped gemm launch");
   }
   if (!ws) {

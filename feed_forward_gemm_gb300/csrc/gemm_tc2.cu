@@ -19,6 +19,11 @@
 //   tempty[b]  (even CTA) 256 arrivals: every epilogue thread of both CTAs.
 // Cluster barriers bracket the kernel so neither CTA leaves while the other may still touch
 // its shared memory or TMEM. Every mbarrier wait is bounded.
+//
+// GROUPED (mixture of experts): as in the single-SM kernel, the rows of A are grouped by expert
+// with the E + 1 offsets read on the device, tiles walk (group 256-row tile, N tile), each CTA
+// loading its 128 rows from the group's first row and the expert's weight slice through a
+// 3-D map, and the epilogue stores rows directly, skipping those past the group.
 #include "activation.cuh"
 #include "gemm_epilogue.cuh"
 #include "internal.h"
@@ -60,16 +65,30 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, in
   tn = r / gm;
 }
 
+// Tile t of a GROUPED launch: expert e, first row of the 256-row tile, rows in it, N tile.
+__device__ __forceinline__ void pair_group_tile(int t, int num_n, const int* s_off,
+                                                const int* s_mt, int& e, int& row0, int& rows,
+                                                int& tn) {
+  const int gm = t / num_n;
+  tn = t - gm * num_n;
+  e = 0;
+  while (s_mt[e + 1] <= gm) ++e;
+  row0 = s_off[e] + (gm - s_mt[e]) * 256;
+  rows = min(256, s_off[e + 1] - row0);
+}
+
 }  // namespace
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool GROUPED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmY,
                     const __nv_bfloat16* __restrict__ bias, int M, int N_out, int K,
-                    int gelu_mode, int group, int* status, uint64_t timeout_ns) {
+                    int gelu_mode, int group, int* status, uint64_t timeout_ns,
+                    const int* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ ydir,
+                    int ldy) {
   using C = PairCfg<BN>;
   constexpr int kPairStages = C::STAGES;
   constexpr int kPairStage = C::STAGE;
@@ -120,10 +139,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   pdl_wait_primary();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const int num_m = (M + 2 * 128 - 1) / (2 * 128);
+  int num_m = (M + 2 * 128 - 1) / (2 * 128);
   const int num_n = (N_out + BN_OUT - 1) / BN_OUT;
-  const int num_tiles = num_m * num_n;
   const int num_kb = (K + kPairBK - 1) / kPairBK;
+  // GROUPED: token offsets and per-group prefix of 256-row tiles, in the (unused) staging area
+  int* s_off = reinterpret_cast<int*>(stg_all);
+  int* s_mt = s_off + (kMoeMaxExperts + 1);
+  if constexpr (GROUPED) {
+    for (int i = threadIdx.x; i <= E; i += kPairThreads) s_off[i] = min(max(__ldcg(offsets + i), 0), M);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      s_mt[0] = 0;
+      for (int g = 0; g < E; ++g) {
+        s_off[g + 1] = max(s_off[g + 1], s_off[g]);   // a falling offset makes the group empty
+        acc += (s_off[g + 1] - s_off[g] + 255) / 256;
+        s_mt[g + 1] = acc;
+      }
+    }
+    __syncthreads();
+    num_m = s_mt[E];
+  }
+  const int num_tiles = num_m * num_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -134,9 +171,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t issued_mask = 0, last_phase_mask = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        int tm, tn;
-        pair_tile_coords(t, num_m, num_n, group, tm, tn);
-        const int a_row = tm * 256 + static_cast<int>(rank) * 128;
+        int tm = 0, tn, ge = 0, grow = 0, grows = 0;
+        if constexpr (GROUPED)
+          pair_group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+        else
+          pair_tile_coords(t, num_m, num_n, group, tm, tn);
+        const int a_row = (GROUPED ? grow : tm * 256) + static_cast<int>(rank) * 128;
         const CUtensorMap* bmap = &tmB0;
         int b_row;
         if (EPI == EPI_GEGLU) {
@@ -155,7 +195,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
           const uint32_t fb = full0 + static_cast<uint32_t>(stage * 8);
           tma_load_2d_pair(sA, &tmA, fb, kb * kPairBK, a_row);
-          tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
+          if constexpr (GROUPED)
+            tma_load_3d_pair(sB, bmap, fb, kb * kPairBK, b_row, ge);
+          else
+            tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
           issued_mask |= 1u << stage;
           last_phase_mask = (last_phase_mask & ~(1u << stage)) | (phase << stage);
           if (++stage == kPairStages) {
@@ -219,8 +262,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int sb = 0;
     int it = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++it) {
-      int tm, tn;
-      pair_tile_coords(t, num_m, num_n, group, tm, tn);
+      int tm = 0, tn, ge = 0, grow = 0, grows = 0;
+      if constexpr (GROUPED)
+        pair_group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+      else
+        pair_tile_coords(t, num_m, num_n, group, tm, tn);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       const bool ok = mbar_wait(&tfull[buf], use, status, SITE_EPI_TMEM_FULL, timeout_ns);
@@ -228,9 +274,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      const int row0 = tm * 256 + static_cast<int>(rank) * 128 + wq * 32;
-      epilogue_cols<BN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
-                                          &tmY, bias, gelu_mode);
+      if constexpr (GROUPED) {
+        const int r = static_cast<int>(rank) * 128 + wq * 32 + lane;
+        epilogue_rows_direct<BN, BN_OUT, EPI>(t_row, lane, r < grows,
+                                              ydir + static_cast<size_t>(grow + r) * ldy,
+                                              tn * BN_OUT, N_out, bias, gelu_mode);
+      } else {
+        const int row0 = tm * 256 + static_cast<int>(rank) * 128 + wq * 32;
+        epilogue_cols<BN, BN_OUT, EPI>(t_row, stg, sb, lane, row0, tn * BN_OUT, M, N_out,
+                                       &tmY, bias, gelu_mode);
+      }
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf * 8));
     }
@@ -247,10 +300,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool GROUPED = false>
 static cudaError_t launch_pair(const GemmLaunch& L) {
   using C = PairCfg<BN>;
-  auto kern = gemm_tc2_kernel<BN, EPI>;
+  auto kern = gemm_tc2_kernel<BN, EPI, GROUPED>;
   static SmemAttrCache cache;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM, cache);
   if (e != cudaSuccess) return e;
@@ -270,7 +323,8 @@ static cudaError_t launch_pair(const GemmLaunch& L) {
   group = group < 2 ? 2 : (group > 16 ? 16 : group);
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB0, L.tmB1, L.tmY,
                             static_cast<const __nv_bfloat16*>(L.bias), L.M, L.N_out, L.K,
-                            L.gelu_mode, group, L.status, L.timeout_ns);
+                            L.gelu_mode, group, L.status, L.timeout_ns, L.offsets, L.groups,
+                            static_cast<__nv_bfloat16*>(L.ydir), L.ldy);
 }
 
 cudaError_t gemm_tc2_launch(const GemmLaunch& L) {
@@ -283,9 +337,20 @@ cudaError_t gemm_tc2_launch(const GemmLaunch& L) {
   }
 }
 
+cudaError_t gemm_tc2_grouped_launch(const GemmLaunch& L) {
+  if (L.grid < 2 || (L.grid & 1) || L.groups < 1 || L.groups > kMoeMaxExperts || !L.offsets ||
+      !L.ydir || L.bn != 256)
+    return cudaErrorInvalidValue;
+  switch (L.epi) {
+    case EPI_BIAS: return launch_pair<256, EPI_BIAS, true>(L);
+    case EPI_GEGLU: return launch_pair<256, EPI_GEGLU, true>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 // Largest number of co-resident CTA pairs (queried once per device by the host).
 cudaError_t gemm_tc2_max_pairs(int* pairs) {
-  auto kern = gemm_tc2_kernel<256, EPI_BIAS>;
+  auto kern = gemm_tc2_kernel<256, EPI_BIAS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PairCfg<256>::SMEM);
   if (e != cudaSuccess) return e;

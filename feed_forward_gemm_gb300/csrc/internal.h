@@ -95,6 +95,8 @@ cudaError_t gemm_tc_grouped_launch(const GemmLaunch& L);
 // grid = 2 x pairs.
 cudaError_t gemm_tc2_launch(const GemmLaunch& L);
 cudaError_t gemm_tc2_max_pairs(int* pairs);
+// The CTA-pair kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).
+cudaError_t gemm_tc2_grouped_launch(const GemmLaunch& L);
 // Dynamic shared memory a GEMM configuration needs (0 if the configuration does not exist).
 int gemm_tc_smem_bytes(int epi, int bn);
 

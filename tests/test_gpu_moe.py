@@ -52,6 +52,22 @@ def test_moe_vs_oracle(counts):
     assert_parity(y, oracle.moe_geglu(x, offsets, Wg, Wu, Wd), f"moe {counts}")
 
 
+def test_moe_single_sm_tiles_vs_oracle():
+    """The grouped single-SM kernel (tile policy forced to single-SM tiles) on uneven groups."""
+    counts = [130, 0, 257, 1, 300, 12]
+    E, D, H = len(counts), 512, 768
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    T = int(offsets[-1])
+    x = bits((T, D), 2.0)
+    Wg, Wu, Wd = experts(E, D, H)
+    try:
+        fm.fmlp_set_tile_policy(fm.FMLP_TILES_SINGLE)
+        y = run(x, offsets, Wg, Wu, Wd, T, D, H, E)
+    finally:
+        fm.fmlp_set_tile_policy(fm.FMLP_TILES_AUTO)
+    assert_parity(y, oracle.moe_geglu(x, offsets, Wg, Wu, Wd), "moe single-SM tiles")
+
+
 def test_moe_one_expert_and_identical_experts_are_the_plain_block():
     T, D, H = 300, 256, 768
     x = bits((T, D), 2.0)

@@ -43,7 +43,7 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="headline only")
     p.add_argument("--cpu-sample-rows", type=int, default=0)
     p.add_argument("--profile-kernel", default=None,
-                   choices=["gate_up", "down", "geglu", "mlp_up", "mlp", "linear"],
+                   choices=["gate_up", "down", "geglu", "mlp_up", "mlp", "linear", "moe"],
                    help="profiling aid: launch one entry point --launches times on random "
                         "inputs of --shape and exit (no timing, no JSON)")
     p.add_argument("--shape", default="8192,8192,8192", help="T,D,H for --profile-kernel")
@@ -594,6 +594,7 @@ def run_reference(args, dist: Dist):
 
 def run_profile_case(args):
     """Launch one entry point a few times on device-random inputs (for ncu captures)."""
+    import numpy as np
     import torch
 
     import feed_forward_gemm_gb300 as fm
@@ -613,6 +614,15 @@ def run_profile_case(args):
     mid = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
     k = args.profile_kernel
+    if k == "moe":
+        # 8 experts with the benchmark's uneven shares of the T rows
+        share = np.array([16, 12, 10, 8, 6, 5, 4, 3], dtype=np.float64)
+        cnt = np.floor(share / share.sum() * T).astype(np.int64)
+        cnt[0] += T - cnt.sum()
+        moe_off = torch.tensor(np.concatenate([[0], np.cumsum(cnt)]), dtype=torch.int32,
+                               device=dev)
+        moe_g, moe_u = rnd(8, H, D, scale=D ** -0.5), rnd(8, H, D, scale=D ** -0.5)
+        moe_d = rnd(8, D, H, scale=H ** -0.5)
     fm.fmlp_set_tile_policy({"auto": fm.FMLP_TILES_AUTO, "single": fm.FMLP_TILES_SINGLE,
                              "pair": fm.FMLP_TILES_PAIR}[args.tiles])
     for _ in range(args.launches):
@@ -629,6 +639,9 @@ def run_profile_case(args):
                              mid.numel() * 2)
         elif k == "linear":
             fm.fmlp_linear_bias(x, W1, b1, mid, T, D, H)
+        elif k == "moe":
+            fm.fmlp_moe_geglu(x, moe_off, moe_g, moe_u, moe_d, y, T, D, H, 8, mid,
+                              mid.numel() * 2)
     torch.cuda.synchronize()
     st = fm.fmlp_device_status()
     if st != fm.FMLP_OK:

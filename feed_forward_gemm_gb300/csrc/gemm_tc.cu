@@ -32,7 +32,8 @@
 // [offsets[e], offsets[e+1]) belonging to expert e, whose weights are slice e of a 3-D tensor
 // [E, N, K]. One launch serves every expert: each CTA reads the offsets after the dependency
 // wait (a router kernel may have written them just before), counts each group's 128-row
-// tiles, and walks tiles ordered by (group row tile, N tile). A loads start at the group's
+// tiles, and walks each group's tiles row tile fastest, so the CTAs in flight share one
+// weight panel of the expert and its few token rows in L2. A loads start at the group's
 // row; B loads take the expert's slice through a 3-D tensor map; the epilogue stores rows
 // directly and skips the rows past the group's end, which the 128-row tile computed
 // from the next group's tokens.
@@ -76,14 +77,16 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& tm
   tn = r / gm;
 }
 
-// Group g of a GROUPED launch: tile t -> expert e, first row, rows in the tile, N tile.
-__device__ __forceinline__ void group_tile(int t, int num_n, const int* s_off, const int* s_mt,
-                                           int& e, int& row0, int& rows, int& tn) {
-  const int gm = t / num_n;
-  tn = t - gm * num_n;
+// Tile t of a GROUPED launch (s_tp: prefix of the groups' tile counts) -> expert e, first row,
+// rows in the tile, N tile; within a group the row tile runs fastest.
+__device__ __forceinline__ void group_tile(int t, const int* s_off, const int* s_tp, int& e,
+                                           int& row0, int& rows, int& tn) {
   e = 0;
-  while (s_mt[e + 1] <= gm) ++e;
-  row0 = s_off[e] + (gm - s_mt[e]) * kBM;
+  while (s_tp[e + 1] <= t) ++e;
+  const int local = t - s_tp[e];
+  const int mt_e = (s_off[e + 1] - s_off[e] + kBM - 1) / kBM;
+  tn = local / mt_e;
+  row0 = s_off[e] + (local - tn * mt_e) * kBM;
   rows = min(kBM, s_off[e + 1] - row0);
 }
 
@@ -141,28 +144,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait_primary();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  int num_m = (M + kBM - 1) / kBM;
+  const int num_m = (M + kBM - 1) / kBM;
   const int num_n = (N_out + C::BN_OUT - 1) / C::BN_OUT;
   const int num_kb = (K + kBK - 1) / kBK;
-  // GROUPED: token offsets and per-group prefix of 128-row tiles, in the (unused) staging area
+  // GROUPED: token offsets and the prefix of the groups' tile counts, in the (unused) staging
+  // area
   int* s_off = reinterpret_cast<int*>(stg_all);
-  int* s_mt = s_off + (kMoeMaxExperts + 1);
+  int* s_tp = s_off + (kMoeMaxExperts + 1);
+  int grouped_tiles = 0;
   if constexpr (GROUPED) {
     for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = min(max(__ldcg(offsets + i), 0), M);
     __syncthreads();
     if (threadIdx.x == 0) {
       int acc = 0;
-      s_mt[0] = 0;
+      s_tp[0] = 0;
       for (int g = 0; g < E; ++g) {
         s_off[g + 1] = max(s_off[g + 1], s_off[g]);   // a falling offset makes the group empty
-        acc += (s_off[g + 1] - s_off[g] + kBM - 1) / kBM;
-        s_mt[g + 1] = acc;
+        acc += (s_off[g + 1] - s_off[g] + kBM - 1) / kBM * num_n;
+        s_tp[g + 1] = acc;
       }
     }
     __syncthreads();
-    num_m = s_mt[E];
+    grouped_tiles = s_tp[E];
   }
-  const int num_tiles = num_m * num_n;
+  const int num_tiles = GROUPED ? grouped_tiles : num_m * num_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         int tm = 0, tn, ge = 0, grow = 0, grows = 0;
         if constexpr (GROUPED)
-          group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+          group_tile(t, s_off, s_tp, ge, grow, grows, tn);
         else
           tile_coords(t, num_m, num_n, tm, tn);
         const int a_row = GROUPED ? grow : tm * kBM;
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int tm = 0, tn, ge = 0, grow = 0, grows = 0;
       if constexpr (GROUPED)
-        group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+        group_tile(t, s_off, s_tp, ge, grow, grows, tn);
       else
         tile_coords(t, num_m, num_n, tm, tn);
       const int buf = it & 1;

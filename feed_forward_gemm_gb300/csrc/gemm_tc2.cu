@@ -21,7 +21,7 @@
 // its shared memory or TMEM. Every mbarrier wait is bounded.
 //
 // GROUPED (mixture of experts): as in the single-SM kernel, the rows of A are grouped by expert
-// with the E + 1 offsets read on the device, tiles walk (group 256-row tile, N tile), each CTA
+// with the E + 1 offsets read on the device, each group's tiles walk 256-row tile fastest, each CTA
 // loading its 128 rows from the group's first row and the expert's weight slice through a
 // 3-D map, and the epilogue stores rows directly, skipping those past the group.
 #include "activation.cuh"
@@ -65,15 +65,17 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, in
   tn = r / gm;
 }
 
-// Tile t of a GROUPED launch: expert e, first row of the 256-row tile, rows in it, N tile.
-__device__ __forceinline__ void pair_group_tile(int t, int num_n, const int* s_off,
-                                                const int* s_mt, int& e, int& row0, int& rows,
-                                                int& tn) {
-  const int gm = t / num_n;
-  tn = t - gm * num_n;
+// Tile t of a GROUPED launch (s_tp: prefix of the groups' tile counts) -> expert e, first row
+// of the 256-row tile, rows in it, N tile; within a group the row tile runs fastest, so the
+// pairs in flight share one weight panel of the expert.
+__device__ __forceinline__ void pair_group_tile(int t, const int* s_off, const int* s_tp, int& e,
+                                                int& row0, int& rows, int& tn) {
   e = 0;
-  while (s_mt[e + 1] <= gm) ++e;
-  row0 = s_off[e] + (gm - s_mt[e]) * 256;
+  while (s_tp[e + 1] <= t) ++e;
+  const int local = t - s_tp[e];
+  const int mt_e = (s_off[e + 1] - s_off[e] + 255) / 256;
+  tn = local / mt_e;
+  row0 = s_off[e] + (local - tn * mt_e) * 256;
   rows = min(256, s_off[e + 1] - row0);
 }
 
@@ -139,28 +141,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   pdl_wait_primary();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  int num_m = (M + 2 * 128 - 1) / (2 * 128);
+  const int num_m = (M + 2 * 128 - 1) / (2 * 128);
   const int num_n = (N_out + BN_OUT - 1) / BN_OUT;
   const int num_kb = (K + kPairBK - 1) / kPairBK;
-  // GROUPED: token offsets and per-group prefix of 256-row tiles, in the (unused) staging area
+  // GROUPED: token offsets and the prefix of the groups' tile counts, in the (unused) staging
+  // area
   int* s_off = reinterpret_cast<int*>(stg_all);
-  int* s_mt = s_off + (kMoeMaxExperts + 1);
+  int* s_tp = s_off + (kMoeMaxExperts + 1);
+  int grouped_tiles = 0;
   if constexpr (GROUPED) {
     for (int i = threadIdx.x; i <= E; i += kPairThreads) s_off[i] = min(max(__ldcg(offsets + i), 0), M);
     __syncthreads();
     if (threadIdx.x == 0) {
       int acc = 0;
-      s_mt[0] = 0;
+      s_tp[0] = 0;
       for (int g = 0; g < E; ++g) {
         s_off[g + 1] = max(s_off[g + 1], s_off[g]);   // a falling offset makes the group empty
-        acc += (s_off[g + 1] - s_off[g] + 255) / 256;
-        s_mt[g + 1] = acc;
+        acc += (s_off[g + 1] - s_off[g] + 255) / 256 * num_n;
+        s_tp[g + 1] = acc;
       }
     }
     __syncthreads();
-    num_m = s_mt[E];
+    grouped_tiles = s_tp[E];
   }
-  const int num_tiles = num_m * num_n;
+  const int num_tiles = GROUPED ? grouped_tiles : num_m * num_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -173,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         int tm = 0, tn, ge = 0, grow = 0, grows = 0;
         if constexpr (GROUPED)
-          pair_group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+          pair_group_tile(t, s_off, s_tp, ge, grow, grows, tn);
         else
           pair_tile_coords(t, num_m, num_n, group, tm, tn);
         const int a_row = (GROUPED ? grow : tm * 256) + static_cast<int>(rank) * 128;
@@ -264,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     for (int t = pair; t < num_tiles; t += npairs, ++it) {
       int tm = 0, tn, ge = 0, grow = 0, grows = 0;
       if constexpr (GROUPED)
-        pair_group_tile(t, num_n, s_off, s_mt, ge, grow, grows, tn);
+        pair_group_tile(t, s_off, s_tp, ge, grow, grows, tn);
       else
         pair_tile_coords(t, num_m, num_n, group, tm, tn);
       const int buf = it & 1;

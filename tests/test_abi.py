@@ -206,3 +206,16 @@ def test_moe_validation(lib):
     assert call(T=0, x=0, y=0) == fm.FMLP_OK
     assert fm.fmlp_moe_geglu_workspace_size(100, 512, 1024) == 100 * 1024 * 2
     assert fm.fmlp_moe_geglu_workspace_size(0, 512, 1024) == 0
+
+
+def test_decode_crossover_is_pure_host(lib):
+    """The GEMV serves one token, and two when the call's weights are small (<= 16 MiB); the
+    tcgen05 kernels (the few-token one below 129 tokens) serve the rest."""
+    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(2, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(1, 768, 3072) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_GEMV      # 14 MB of weights
+    assert fm.fmlp_geglu_plan(3, 768, 3072) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_linear_plan(2, 4096, 4096) == fm.FMLP_PLAN_TC       # 33.6 MB
+    assert fm.fmlp_linear_plan(2, 256, 64) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_linear_plan(1, 4104, 520) == fm.FMLP_PLAN_TC        # K not a multiple of 256

@@ -86,9 +86,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
-def kernel_fingerprint(names=("gemm_tc.cu", "gemm_tc2.cu", "gemm_epilogue.cuh", "ptx.cuh",
+def kernel_fingerprint(names=("gemm_tc2.cu", "gemm_epilogue.cuh", "ptx.cuh",
                              "activation.cuh")) -> str:
-    """Short hash of the kernel sources a profile was taken on."""
+    """Short hash of the sources the profiled CTA-pair GEMM kernels are compiled from (their
+    file and the device headers it includes), recorded beside a profile's counters."""
     h = hashlib.sha256()
     for n in names:
         with open(os.path.join(CSRC, n), "rb") as fh:

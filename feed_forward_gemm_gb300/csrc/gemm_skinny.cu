@@ -214,7 +214,8 @@ static int skinny_smem(int nmat, int tpad, int stages) {
   return 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
 }
 
-int gemm_skinny_stages(int nmat, int tpad) {
+// Pipeline stages for nmat weight matrices and tpad token rows (0: does not fit).
+static int gemm_skinny_stages(int nmat, int tpad) {
   const int stage_bytes = nmat * kSkA + tpad * kSkBK * 2;
   int stages = (192 * 1024) / stage_bytes;
   if (stages > 8) stages = 8;

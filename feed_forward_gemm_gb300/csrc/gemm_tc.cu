@@ -334,20 +334,6 @@ static cudaError_t launch_one(const GemmLaunch& L) {
                             static_cast<__nv_bfloat16*>(L.ydir), L.ldy);
 }
 
-int gemm_tc_smem_bytes(int epi, int bn) {
-  switch (epi * 1000 + bn) {
-    case EPI_BIAS * 1000 + 64: return Cfg<64, EPI_BIAS>::SMEM_BYTES;
-    case EPI_BIAS * 1000 + 128: return Cfg<128, EPI_BIAS>::SMEM_BYTES;
-    case EPI_BIAS * 1000 + 256: return Cfg<256, EPI_BIAS>::SMEM_BYTES;
-    case EPI_BIAS_GELU * 1000 + 64: return Cfg<64, EPI_BIAS_GELU>::SMEM_BYTES;
-    case EPI_BIAS_GELU * 1000 + 128: return Cfg<128, EPI_BIAS_GELU>::SMEM_BYTES;
-    case EPI_BIAS_GELU * 1000 + 256: return Cfg<256, EPI_BIAS_GELU>::SMEM_BYTES;
-    case EPI_GEGLU * 1000 + 128: return Cfg<128, EPI_GEGLU>::SMEM_BYTES;
-    case EPI_GEGLU * 1000 + 256: return Cfg<256, EPI_GEGLU>::SMEM_BYTES;
-    default: return 0;
-  }
-}
-
 cudaError_t gemm_tc_launch(const GemmLaunch& L) {
   switch (L.epi * 1000 + L.bn) {
     case EPI_BIAS * 1000 + 64: return launch_one<64, EPI_BIAS>(L);

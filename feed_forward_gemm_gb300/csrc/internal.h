@@ -85,8 +85,6 @@ struct SkinnyLaunch {
   uint64_t timeout_ns;
 };
 cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
-// Pipeline stages for nmat weight matrices and tpad token rows (0: does not fit).
-int gemm_skinny_stages(int nmat, int tpad);
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
 // The single-SM kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).
@@ -97,8 +95,6 @@ cudaError_t gemm_tc2_launch(const GemmLaunch& L);
 cudaError_t gemm_tc2_max_pairs(int* pairs);
 // The CTA-pair kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).
 cudaError_t gemm_tc2_grouped_launch(const GemmLaunch& L);
-// Dynamic shared memory a GEMM configuration needs (0 if the configuration does not exist).
-int gemm_tc_smem_bytes(int epi, int bn);
 
 // Weight-streaming GEMV for T <= kGemvMaxT tokens (decode; the plans use it for one or two).
 constexpr int kGemvMaxT = 4;

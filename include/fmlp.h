@@ -15,11 +15,16 @@
  *                      pointwise pass; here it never leaves the GEMM).
  *   fmlp_mlp_gelu      Linear -> GELU -> Linear with biases, y = W2 GELU(W1 x + b1) + b2
  *                      (ainews.cool fused-MLP article, technical deep-dive and benchmark
- *                      sections: one launch instead of three at batch 1).
+ *                      sections: one launch instead of three at batch 1); ReLU may replace
+ *                      the GELU (the same article's two-layer ReLU MLP).
+ *   fmlp_moe_geglu     a mixture of experts, each a GeGLU block over the tokens routed to it
+ *                      (the same article's MoE note), one launch per stage over all experts.
+ *   fmlp_linear_bias_strided  fmlp_linear_bias on row-strided views (section "What's the
+ *                      transpose doing?").
  *
  * Common conventions
- *   - Tensors are dense, row-major (last index fastest), contiguous, bfloat16 bit patterns in
- *     device memory. x is [T, in]; weights use the nn.Linear layout [out, in]; biases [out].
+ *   - Tensors are dense, row-major (last index fastest), contiguous (except the views of
+ *     fmlp_linear_bias_strided), bfloat16 bit patterns in device memory. x is [T, in]; weights use the nn.Linear layout [out, in]; biases [out].
  *     T is the token count batch*seq (section "Why are there two kinds of GEMM kernels?").
  *   - Accumulation is fp32. The bias is added in fp32 before the activation. The output and
  *     the one intermediate (m or h) are each rounded to bf16 once, round-to-nearest-even.

@@ -110,11 +110,12 @@ def gelu(x: np.ndarray, mode: int = GELU_TANH) -> np.ndarray:
 
 
 
-def moe_geglu(x, offsets, Wg, Wu, Wd, want_m=False, nthreads=None):
+def moe_geglu(x, offsets, Wg, Wu, Wd, want_m=False, nthreads=None, rows=None):
     """Mixture-of-experts feed-forward (the ainews.cool article's MoE note: every expert is an
     MLP): tokens arrive grouped by expert, rows [offsets[e], offsets[e+1]) of x go through
     expert e's GeGLU block with Wg[e], Wu[e] [H, D] and Wd[e] [D, H]. Each expert's rows are
-    exactly geglu() on those rows; nothing else is computed."""
+    exactly geglu() on those rows; nothing else is computed. rows: optional sorted token-row
+    indices; then only those rows are computed and returned, in that order."""
     x = _u16(x)
     T, D = x.shape
     offsets = np.asarray(offsets, dtype=np.int64)
@@ -122,14 +123,19 @@ def moe_geglu(x, offsets, Wg, Wu, Wd, want_m=False, nthreads=None):
     if E < 1 or offsets[0] != 0 or offsets[-1] != T or np.any(np.diff(offsets) < 0):
         raise ValueError("offsets must rise from 0 to T")
     H = Wg.shape[1]
-    y = np.empty((T, D), dtype=np.uint16)
-    m = np.empty((T, H), dtype=np.uint16)
+    sel = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    if sel.size and (np.any(np.diff(sel) <= 0) or sel[0] < 0 or sel[-1] >= T):
+        raise ValueError("rows must be sorted, unique and inside [0, T)")
+    y = np.empty((sel.size, D), dtype=np.uint16)
+    m = np.empty((sel.size, H), dtype=np.uint16)
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
-        if b == a:
+        lo, hi = np.searchsorted(sel, a), np.searchsorted(sel, b)
+        if b == a or hi == lo:
             continue
-        ye, me = geglu(x[a:b], Wg[e], Wu[e], Wd[e], want_m=True, nthreads=nthreads)
-        y[a:b], m[a:b] = ye, me
+        ye, me = geglu(x[a:b], Wg[e], Wu[e], Wd[e], want_m=True, nthreads=nthreads,
+                       rows=sel[lo:hi] - a)
+        y[lo:hi], m[lo:hi] = ye, me
     return (y, m) if want_m else y
 
 def linear(x, W, b, rows=None, nthreads=None, want_acc=False):

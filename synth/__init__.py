@@ -189,6 +189,38 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class MoeWorkload(Workload):
+    """E experts, each a GeGLU block; the T token rows arrive grouped by expert, `counts[e]`
+    rows for expert e (a fixed routing layout: no trained router exists here)."""
+    E: int = 1
+    counts: tuple = ()
+
+    def offsets(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.counts)]).astype(np.int32)
+
+    def flops(self) -> int:
+        return 3 * 2 * self.T * self.D * self.H
+
+
+def moe_workload(name: str, cid: int, D: int, H: int, counts) -> MoeWorkload:
+    E, T = len(counts), int(sum(counts))
+    return MoeWorkload(name, cid, "moe_geglu", T, D, H, D, (
+        TensorSpec("x", (T, D), "normal", 0.0, 0),
+        TensorSpec("Wg", (E, H, D), "uniform", _lin_bound(D), 1),
+        TensorSpec("Wu", (E, H, D), "uniform", _lin_bound(D), 2),
+        TensorSpec("Wd", (E, D, H), "uniform", _lin_bound(H), 3),
+    ), "tanh", E, tuple(int(c) for c in counts))
+
+
+# A Mixtral-shaped mixture-of-experts layer (the ainews.cool article's MoE note names Mixtral
+# 8x7B): 8 GeGLU experts, D 4096, H 14336, 16,384 routed token rows in uneven groups.
+MOE_WORKLOADS = {
+    "moe_geglu_8x4096x14336": moe_workload("moe_geglu_8x4096x14336", 6, 4096, 14336,
+                                           (4096, 3072, 2560, 2048, 1536, 1280, 1024, 768)),
+}
+
+
 def bf16_bits_to_f32(a: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to float32 values (exact)."""
     return (a.astype(np.uint32) << 16).view(np.float32)

@@ -74,6 +74,36 @@ def torch_mlp_f64(x, W1, b1, W2, b2, approximate: str):
     return y.numpy(), h_bits
 
 
+def _rne_t(t: torch.Tensor) -> torch.Tensor:
+    """Round a float64 tensor to bf16 values with the independent rounding above."""
+    return torch.from_numpy(bits_to_f64(rne_bf16_array(t.numpy())))
+
+
+def torch_geglu_eager_f64(x, Wg, Wu, Wd):
+    """The page's SimpleGeGLUMLP as eager PyTorch runs it in bf16: every tensor the module
+    materialises (g, u, gelu(g), m) is rounded to bf16; products and sums in float64 by torch.
+    Returns (y_before_rounding, m_bits)."""
+    xf, wg, wu, wd = t64(x), t64(Wg), t64(Wu), t64(Wd)
+    g = _rne_t(torch.nn.functional.linear(xf, wg))
+    u = _rne_t(torch.nn.functional.linear(xf, wu))
+    h = _rne_t(torch.nn.functional.gelu(g, approximate="tanh"))
+    m = _rne_t(h * u)
+    y = torch.nn.functional.linear(m, wd)
+    return y.numpy(), rne_bf16_array(m.numpy())
+
+
+def torch_mlp_eager_f64(x, W1, b1, W2, b2, approximate: str):
+    """Linear -> activation -> Linear as eager PyTorch runs it in bf16: the first Linear's
+    output (bias included) and the activation's output are each rounded to bf16.
+    Returns (y_before_rounding, h_bits)."""
+    xf, w1, w2 = t64(x), t64(W1), t64(W2)
+    z = _rne_t(torch.nn.functional.linear(xf, w1, None if b1 is None else t64(b1)))
+    h = _rne_t(torch.relu(z) if approximate == "relu"
+               else torch.nn.functional.gelu(z, approximate=approximate))
+    y = torch.nn.functional.linear(h, w2, None if b2 is None else t64(b2))
+    return y.numpy(), rne_bf16_array(h.numpy())
+
+
 def parity_stats(y_bits: np.ndarray, ref_bits: np.ndarray) -> dict:
     y = bits_to_f64(y_bits)
     r = bits_to_f64(ref_bits)

@@ -104,3 +104,29 @@ def test_moe_offsets_written_just_before_and_same_bits():
         outs.append(to_host(y))
     assert all(np.array_equal(o, outs[0]) for o in outs[1:])
     assert_parity(outs[0], oracle.moe_geglu(x, offsets, Wg, Wu, Wd), "moe after routing")
+
+
+def test_moe_mixtral_shaped_layer_at_the_benchmarked_size():
+    """The benchmarked layer: 8 experts, D 4096, H 14336, 16,384 routed rows in groups of
+    768..4096 (seeded synth inputs, the benchmark's own). Long K (64 K steps per tile) and
+    groups spanning many 256-row tiles; 256 seeded rows of every expert group against the
+    oracle."""
+    import synth
+    w = synth.MOE_WORKLOADS["moe_geglu_8x4096x14336"]
+    t = w.generate()
+    off = w.offsets()
+    dx, dg, du, dd = (to_dev(t[k]) for k in ("x", "Wg", "Wu", "Wd"))
+    y = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=DEV)
+    ws = workspace(fm.fmlp_moe_geglu_workspace_size(w.T, w.D, w.H))
+    fm.fmlp_moe_geglu(dx, torch.tensor(off, dtype=torch.int32, device=DEV), dg, du, dd, y, w.T,
+                      w.D, w.H, w.E, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
+    pick = np.random.default_rng(2024)
+    rows = np.sort(np.concatenate([
+        off[e] + pick.choice(off[e + 1] - off[e], 256, replace=False) for e in range(w.E)]))
+    ref = oracle.moe_geglu(t["x"], off, t["Wg"], t["Wu"], t["Wd"], rows=rows)
+    got = to_host(y)[rows]
+    for e in range(w.E):
+        sel = (rows >= off[e]) & (rows < off[e + 1])
+        assert_parity(got[sel], ref[sel], f"mixtral-shaped layer, expert {e}")

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import (bits_to_f64, f64_to_bits_via_torch, parity_stats, rne_bf16_array, t64,
+from helpers import (bits_to_f64, f64_to_bits_via_torch, parity_stats, rne_bf16_array, t64, torch_geglu_eager_f64, torch_mlp_eager_f64,
                      rne_bf16_bits, torch_geglu_f64, torch_mlp_f64)
 import synth
 
@@ -195,6 +195,42 @@ def test_geglu_eager_and_fused_rounding_both_within_tolerance():
     assert s["mismatch_bits"] > 0    # the two readings do differ
 
 
+@pytest.mark.parametrize("T,D,H", [(3, 16, 72), (33, 64, 48)])
+def test_geglu_eager_rounding_vs_torch_module(T, D, H):
+    """The eager-rounding reading (g, u, gelu(g) and m each rounded to bf16, as the eager
+    module materialises them) against torch's float64 evaluation of the page's module with
+    those roundings written out: m bit-equal, y's sum to 1e-12. Dropping any one of the four
+    roundings changes m somewhere, which the bit comparison catches."""
+    x = rand_bits((T, D))
+    Wg, Wu = rand_bits((H, D), 1 / math.sqrt(D)), rand_bits((H, D), 1 / math.sqrt(D))
+    Wd = rand_bits((D, H), 1 / math.sqrt(H))
+    y, acc, m = oracle.geglu(x, Wg, Wu, Wd, eager=True, want_acc=True, want_m=True)
+    ref_y, ref_m = torch_geglu_eager_f64(x, Wg, Wu, Wd)
+    assert np.array_equal(m, ref_m)
+    assert np.max(np.abs(acc - ref_y)) <= 1e-12 * max(1.0, np.abs(ref_y).max())
+    assert np.array_equal(y, rne_bf16_array(acc))
+    _, m_fused = oracle.geglu(x, Wg, Wu, Wd, want_m=True)
+    assert not np.array_equal(m, m_fused)       # the readings differ on these inputs
+
+
+@pytest.mark.parametrize("approx,mode", [("tanh", oracle.GELU_TANH), ("none", oracle.GELU_ERF),
+                                         ("relu", oracle.RELU)])
+def test_mlp_eager_rounding_vs_torch(approx, mode):
+    """Eager reading of Linear -> activation -> Linear: W1 x + b1 rounded to bf16 before the
+    activation, and the activation's output rounded; h bit-equal to torch's float64
+    evaluation with those roundings, y's sum to 1e-12."""
+    T, D, H, Do = 9, 24, 40, 16
+    x = rand_bits((T, D))
+    W1, b1 = rand_bits((H, D), 1 / math.sqrt(D)), rand_bits((H,), 1 / math.sqrt(D))
+    W2, b2 = rand_bits((Do, H), 1 / math.sqrt(H)), rand_bits((Do,), 1 / math.sqrt(H))
+    y, acc, h = oracle.mlp_gelu(x, W1, b1, W2, b2, gelu_mode=mode, eager=True, want_acc=True,
+                                want_h=True)
+    ref_y, ref_h = torch_mlp_eager_f64(x, W1, b1, W2, b2, approx)
+    assert np.array_equal(h, ref_h)
+    assert np.max(np.abs(acc - ref_y)) <= 1e-12 * max(1.0, np.abs(ref_y).max())
+    assert np.array_equal(y, rne_bf16_array(acc))
+
+
 # ---------------------------------------------------------------------------- MLP
 
 def test_relu_matches_torch():
@@ -277,3 +313,20 @@ def test_moe_rejects_bad_offsets():
     for bad in ([0, 9, 8], [1, 4, 8], [0, 5, 3, 8][:3]):
         with pytest.raises(ValueError):
             oracle.moe_geglu(x, bad, W, W, Wd)
+
+
+def test_moe_row_subset_equals_full_rows():
+    """Selecting rows of the mixture-of-experts oracle returns exactly those rows of the full
+    computation (groups with no selected row, and an empty group, included)."""
+    E, D, H = 4, 16, 24
+    counts = [5, 0, 9, 3]
+    T = sum(counts)
+    off = np.concatenate([[0], np.cumsum(counts)])
+    x = rand_bits((T, D))
+    Wg, Wu = rand_bits((E, H, D), 0.25), rand_bits((E, H, D), 0.25)
+    Wd = rand_bits((E, D, H), 0.2)
+    full = oracle.moe_geglu(x, off, Wg, Wu, Wd)
+    rows = np.array([0, 3, 5, 6, 13])
+    assert np.array_equal(oracle.moe_geglu(x, off, Wg, Wu, Wd, rows=rows), full[rows])
+    with pytest.raises(ValueError):
+        oracle.moe_geglu(x, off, Wg, Wu, Wd, rows=np.array([3, 1]))

@@ -19,6 +19,7 @@ from . import _build
 __all__ = [
     "FmlpError", "load", "build", "library_path",
     "fmlp_linear_bias", "fmlp_linear_bias_strided", "fmlp_linear_bias_gelu",
+    "fmlp_geglu_strided", "fmlp_mlp_gelu_strided",
     "fmlp_geglu_gate_up", "fmlp_geglu", "fmlp_moe_geglu", "fmlp_moe_geglu_workspace_size",
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
     "fmlp_geglu_plan", "fmlp_mlp_gelu_plan", "fmlp_linear_plan", "fmlp_gelu_eval",
@@ -28,14 +29,16 @@ __all__ = [
     "FMLP_OK", "FMLP_ERR_NULL", "FMLP_ERR_SHAPE", "FMLP_ERR_ALIGN", "FMLP_ERR_ALIAS",
     "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
     "FMLP_GELU_TANH", "FMLP_GELU_ERF", "FMLP_PLAN_NONE", "FMLP_PLAN_TC",
-    "FMLP_PLAN_FUSED_SMALL", "FMLP_PLAN_GEMV",
+    "FMLP_PLAN_FUSED_SMALL", "FMLP_PLAN_GEMV", "FMLP_PLAN_DECODE", "fmlp_test_decode_overload",
+    "fmlp_test_inject", "FMLP_INJECT_NONE", "FMLP_INJECT_LAUNCH", "FMLP_INJECT_SKIP_LOAD",
 ]
 
 FMLP_OK, FMLP_ERR_NULL, FMLP_ERR_SHAPE, FMLP_ERR_ALIGN, FMLP_ERR_ALIAS = 0, 1, 2, 3, 4
 FMLP_ERR_WORKSPACE, FMLP_ERR_CUDA, FMLP_ERR_DEVICE_TIMEOUT, FMLP_ERR_DEVICE = 5, 6, 7, 8
 FMLP_GELU_TANH, FMLP_GELU_ERF, FMLP_RELU = 0, 1, 2
-FMLP_PLAN_NONE, FMLP_PLAN_TC, FMLP_PLAN_FUSED_SMALL, FMLP_PLAN_GEMV = 0, 1, 2, 3
+FMLP_PLAN_NONE, FMLP_PLAN_TC, FMLP_PLAN_FUSED_SMALL, FMLP_PLAN_GEMV, FMLP_PLAN_DECODE = 0, 1, 2, 3, 4
 FMLP_TILES_AUTO, FMLP_TILES_SINGLE, FMLP_TILES_PAIR = 0, 1, 2
+FMLP_INJECT_NONE, FMLP_INJECT_LAUNCH, FMLP_INJECT_SKIP_LOAD = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +59,9 @@ _SIGNATURES = {
     "fmlp_geglu_gate_up": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fmlp_geglu": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "fmlp_mlp_gelu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _INT, _P, _SZ, _P]),
+    "fmlp_geglu_strided": (_INT, [_P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _SZ, _P]),
+    "fmlp_mlp_gelu_strided": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
+                                     _INT, _P, _SZ, _P]),
     "fmlp_geglu_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fmlp_mlp_gelu_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
     "fmlp_geglu_plan": (_INT, [_I64, _I64, _I64]),
@@ -64,6 +70,8 @@ _SIGNATURES = {
     "fmlp_gelu_eval": (_INT, [_P, _P, _I64, _INT, _P]),
     "fmlp_device_status": (_INT, [_P]),
     "fmlp_test_wait_timeout": (_INT, [_I64, _P]),
+    "fmlp_test_decode_overload": (_INT, [_I64, _I64]),
+    "fmlp_test_inject": (_INT, [_INT, _I64, _I64]),
     "fmlp_status_string": (ctypes.c_char_p, [_INT]),
     "fmlp_last_error": (ctypes.c_char_p, []),
     "fmlp_version": (_INT, []),
@@ -229,6 +237,27 @@ def fmlp_mlp_gelu(x, W1, b1, W2, b2, y, T, D, H, Dout, mode=FMLP_GELU_ERF, ws=No
     return _check(st, "fmlp_mlp_gelu", raise_on_error)
 
 
+def fmlp_geglu_strided(x, Wg, Wu, Wd, y, T, D, H, ws=None, ws_bytes=0, ldx=None, ldy=None,
+                       stream=None, raise_on_error=True):
+    """fmlp_geglu on row-strided views of x and y; ldx/ldy default to the views' row strides."""
+    px, lx = _view(x, ldx)
+    py, ly = _view(y, ldy)
+    st = load().fmlp_geglu_strided(px, lx, _ptr(Wg), _ptr(Wu), _ptr(Wd), py, ly, T, D, H,
+                                   _ptr(ws), int(ws_bytes), _stream(stream))
+    return _check(st, "fmlp_geglu_strided", raise_on_error)
+
+
+def fmlp_mlp_gelu_strided(x, W1, b1, W2, b2, y, T, D, H, Dout, mode=FMLP_GELU_ERF, ws=None,
+                          ws_bytes=0, ldx=None, ldy=None, stream=None, raise_on_error=True):
+    """fmlp_mlp_gelu on row-strided views of x and y; ldx/ldy default to the views' strides."""
+    px, lx = _view(x, ldx)
+    py, ly = _view(y, ldy)
+    st = load().fmlp_mlp_gelu_strided(px, lx, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), py, ly, T,
+                                      D, H, Dout, int(mode), _ptr(ws), int(ws_bytes),
+                                      _stream(stream))
+    return _check(st, "fmlp_mlp_gelu_strided", raise_on_error)
+
+
 def fmlp_geglu_workspace_size(T, D, H) -> int:
     return int(load().fmlp_geglu_workspace_size(T, D, H))
 
@@ -273,6 +302,19 @@ def fmlp_set_tile_policy(policy: int, raise_on_error=True):
 
 def fmlp_device_status(stream=None) -> int:
     return int(load().fmlp_device_status(_stream(stream)))
+
+
+def fmlp_test_inject(kind, count=0, timeout_us=0, raise_on_error=True):
+    """Failure-injection test hook (FMLP_INJECT_*); FMLP_INJECT_NONE clears everything."""
+    st = load().fmlp_test_inject(int(kind), int(count), int(timeout_us))
+    return _check(st, "fmlp_test_inject", raise_on_error)
+
+
+def fmlp_test_decode_overload(extra_ctas, timeout_us, raise_on_error=True):
+    """Test hook: later one-kernel decode launches get extra_ctas CTAs that cannot be resident
+    and a wait limit of timeout_us (0: default); (0, 0) restores normal launches."""
+    st = load().fmlp_test_decode_overload(int(extra_ctas), int(timeout_us))
+    return _check(st, "fmlp_test_decode_overload", raise_on_error)
 
 
 def fmlp_test_wait_timeout(timeout_us, stream=None, raise_on_error=True):

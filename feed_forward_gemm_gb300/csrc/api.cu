@@ -51,7 +51,30 @@ struct DeviceState {
   int major = 0, minor = 0;
   int max_pairs = 0;   // co-resident CTA pairs of the pair GEMM (0: pair kernel unavailable)
   int* status = nullptr;
+  int decode_occ = 0;  // resident decode CTAs per SM (0: the one-kernel decode cannot run)
+  unsigned long long* decode_bar = nullptr;  // grid-barrier counters (kDecodeSlots)
+  // Stream i of this table uses counter i (a fixed table: assigning one allocates nothing).
+  cudaStream_t decode_stream[kDecodeSlots] = {};
+  int decode_streams = 0;
 };
+
+// Test hook of the one-kernel decode: extra CTAs beyond the resident ones, and the wait limit.
+std::atomic<int> g_decode_extra_ctas{0};
+std::atomic<unsigned long long> g_decode_timeout_ns{0};
+
+// Failure-injection test hooks (fmlp_test_inject): launches left to fail on the host, CTA-pair
+// GEMM launches left to skip their first loads, and the wait limit of those launches.
+std::atomic<int> g_inject_launch{0};
+std::atomic<int> g_inject_skip{0};
+std::atomic<unsigned long long> g_inject_timeout_ns{0};
+
+// Takes one unit of an injection counter (true if one was left).
+bool take_injection(std::atomic<int>& n) {
+  int v = n.load(std::memory_order_relaxed);
+  while (v > 0 && !n.compare_exchange_weak(v, v - 1)) {
+  }
+  return v > 0;
+}
 
 std::atomic<int> g_tile_policy{FMLP_TILES_AUTO};
 
@@ -68,6 +91,16 @@ fmlp_status cuda_fail(cudaError_t e, const char* what) {
   set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
   return FMLP_ERR_CUDA;
 }
+
+// Every kernel launch goes through here first: an injected failure (test hook) stands in for
+// a launch that the runtime refused, and nothing is launched.
+#define FMLP_LAUNCH_GUARD(what)                                                   \
+  do {                                                                            \
+    if (take_injection(g_inject_launch)) {                                        \
+      set_error("%s: injected launch failure (fmlp_test_inject)", what);         \
+      return FMLP_ERR_CUDA;                                                       \
+    }                                                                             \
+  } while (0)
 
 // Current device's cached state; checks the architecture once.
 fmlp_status device_state(DeviceState** out) {
@@ -102,6 +135,12 @@ fmlp_status device_state(DeviceState** out) {
       d.max_pairs = 0;
       (void)cudaGetLastError();
     }
+    if (decode_occupancy(&d.decode_occ) != cudaSuccess ||
+        decode_barrier_base(&d.decode_bar) != cudaSuccess) {
+      d.decode_occ = 0;
+      d.decode_bar = nullptr;
+      (void)cudaGetLastError();
+    }
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -119,10 +158,60 @@ fmlp_status device_state(DeviceState** out) {
   return FMLP_OK;
 }
 
+// Encoded tensor maps, process-wide. A map is a pure function of (address, sizes, strides,
+// box), all of which are in the key, so an entry never goes stale: a buffer freed and
+// reallocated at the same address with the same sizes gets the same, still correct, map.
+// Direct-mapped, kMapCacheSlots entries; a colliding key simply re-encodes and replaces.
+constexpr int kMapCacheSlots = 1024;
+struct MapKey {
+  uintptr_t ptr;
+  uint64_t depth, rows, cols, ld;
+  uint32_t box_rows;
+  uint32_t rank;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && depth == o.depth && rows == o.rows && cols == o.cols && ld == o.ld &&
+           box_rows == o.box_rows && rank == o.rank;
+  }
+};
+struct MapEntry {
+  bool valid = false;
+  MapKey key{};
+  CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCacheSlots];
+
+size_t map_slot(const MapKey& k) {
+  uint64_t h = static_cast<uint64_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+  for (uint64_t v : {k.depth, k.rows, k.cols, k.ld, static_cast<uint64_t>(k.box_rows) << 8 | k.rank})
+    h = (h ^ v) * 0xBF58476D1CE4E5B9ull;
+  return static_cast<size_t>(h >> 40) % kMapCacheSlots;
+}
+
+bool map_lookup(const MapKey& k, CUtensorMap* m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  const MapEntry& e = g_maps[map_slot(k)];
+  if (!e.valid || !(e.key == k)) return false;
+  *m = e.map;
+  return true;
+}
+
+void map_store(const MapKey& k, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[map_slot(k)];
+  e.valid = true;
+  e.key = k;
+  e.map = m;
+}
+
 // Row-major bf16 matrix [rows, cols] -> 2-D tensor map with a {64, box_rows} box, 128B swizzle.
 // ld: row stride in elements (0: rows are packed, ld = cols).
 fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
                      uint32_t box_rows, const char* name, int64_t ld = 0) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), 1, static_cast<uint64_t>(rows),
+                   static_cast<uint64_t>(cols), static_cast<uint64_t>(ld > 0 ? ld : cols),
+                   box_rows, 2};
+  if (map_lookup(key, m)) return FMLP_OK;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld > 0 ? ld : cols) * 2u};
   cuuint32_t box[2] = {64u, box_rows};
@@ -137,12 +226,17 @@ fmlp_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
               static_cast<int>(r));
     return FMLP_ERR_CUDA;
   }
+  map_store(key, *m);
   return FMLP_OK;
 }
 
 // A 3-D map over [depth, rows, cols] bf16 (packed), box {64, box_rows, 1}, 128-byte swizzle.
 fmlp_status make_map3(CUtensorMap* m, const void* ptr, int64_t depth, int64_t rows, int64_t cols,
                       uint32_t box_rows, const char* name) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), static_cast<uint64_t>(depth),
+                   static_cast<uint64_t>(rows), static_cast<uint64_t>(cols),
+                   static_cast<uint64_t>(cols), box_rows, 3};
+  if (map_lookup(key, m)) return FMLP_OK;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(depth)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2u,
@@ -159,6 +253,7 @@ fmlp_status make_map3(CUtensorMap* m, const void* ptr, int64_t depth, int64_t ro
               static_cast<long long>(cols), static_cast<int>(r));
     return FMLP_ERR_CUDA;
   }
+  map_store(key, *m);
   return FMLP_OK;
 }
 
@@ -343,6 +438,7 @@ fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const vo
                           const void* B1, const void* bias, void* Y, int64_t M, int64_t N_out,
                           int64_t K, int gelu_mode, bool pdl, cudaStream_t s, int64_t lda,
                           int64_t ldy) {
+  FMLP_LAUNCH_GUARD("gemm_skinny launch");
   SkinnyLaunch L;
   memset(&L, 0, sizeof L);
   L.tpad = static_cast<int>((M + 31) / 32 * 32);
@@ -379,6 +475,7 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
                         int64_t ldy = 0) {
   if (use_skinny(M))
     return launch_skinny(d, epi, A, B0, B1, bias, Y, M, N_out, K, gelu_mode, pdl, s, lda, ldy);
+  FMLP_LAUNCH_GUARD("gemm launch");
   GemmLaunch L;
   memset(&L, 0, sizeof L);
   const bool geglu = epi == EPI_GEGLU;
@@ -405,6 +502,11 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
   L.status = d.status;
   L.timeout_ns = kWaitTimeoutNs;
   L.grid = ch.grid;
+  if (pair && take_injection(g_inject_skip)) {
+    L.skip_first_load = true;
+    const unsigned long long tmo = g_inject_timeout_ns.load(std::memory_order_relaxed);
+    if (tmo) L.timeout_ns = tmo;
+  }
   const cudaError_t e = pair ? gemm_tc2_launch(L) : gemm_tc_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, pair ? "gemm_tc2 launch" : "gemm_tc launch");
   return FMLP_OK;
@@ -412,15 +514,38 @@ fmlp_status launch_gemm(const DeviceState& d, int epi, const void* A, const void
 
 // ------------------------------------------------------------------------- plans
 
-// The device SM count for host-only plan queries when no device state exists yet; the GEMV
-// smem bound depends on the grid only through rows per CTA, and GB300 has 152 SMs.
-constexpr int kPlanSms = 152;
+// SM count for the host-only plan queries: the current device's (no context is created), or
+// GB300's 152 when no device is visible. The workspace a plan needs never depends on it.
+int plan_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (g_dev[dev].ready) return g_dev[dev].sms;
+    }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      return n;
+  }
+  (void)cudaGetLastError();
+  return 152;
+}
+
+// The one-kernel decode (both layers, one CTA per SM) serves 1..kDecodeMaxT tokens when its
+// token vectors and reduction buffers fit in shared memory.
+bool decode_ok(int64_t T, int64_t D, int64_t H, int64_t Dout, int nmat, int sms) {
+  return T >= 1 && T <= kDecodeMaxT && D >= 8 && D % 8 == 0 && H >= 8 && H % 8 == 0 &&
+         D <= kMaxDim && H <= kMaxDim && Dout >= 1 && Dout <= kMaxDim &&
+         decode_smem_bytes(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
+                           static_cast<int>(Dout), nmat, sms) <= kDecodeMaxSmem;
+}
 
 // Decode crossover, measured on GB300 (CUDA graphs of 20 calls over 5 weight sets): the GEMV
 // wins at one token, and at two when the call's weights are small (16 MiB or less: 9.3 vs
 // 10.1 us for the GPT-2-small-shaped GeGLU); otherwise the few-token tcgen05 kernel wins
 // (4096-wide MLP at 2-4 tokens: 20.3 us against 25.9-33.9 us for the GEMV).
 constexpr int64_t kGemvSmallWeights = int64_t(16) << 20;
+// Below this many weight bytes a few-token GeGLU stays on the single-CTA fused kernel.
+constexpr size_t kSmallDecodeBytes = size_t(1) << 20;
 bool gemv_preferred(int64_t T, int64_t weight_bytes) {
   return T == 1 || (T == 2 && weight_bytes <= kGemvSmallWeights);
 }
@@ -439,26 +564,35 @@ int plan_linear(int64_t T, int64_t in, int64_t out, int sms) {
                                                                               : FMLP_PLAN_TC;
 }
 
+// Whether the single-kernel fused plan takes a block of these sizes. It depends on the shape
+// alone (never on the SM count), so the workspace query and the call agree on whether the
+// intermediate needs a workspace. At decode sizes (1..kDecodeMaxT tokens) the one-kernel
+// decode spreads the weights over every SM; the single-CTA fused kernel only takes tiny ones.
+bool fused_small(int64_t T, int64_t D, int64_t H, int64_t Dout, bool mlp) {
+  const bool shape = mlp ? (D <= kSmallMaxD && Dout <= kSmallMaxD && Dout % 16 == 0 &&
+                            H <= kSmallMaxH)
+                         : (D <= kSmallMaxD && D % 16 == 0 && H <= kSmallMaxH);
+  const size_t wbytes = mlp ? mat_bytes(H, D) + mat_bytes(Dout, H) : 3 * mat_bytes(H, D);
+  return T >= 1 && shape && (T > kDecodeMaxT || wbytes <= kSmallDecodeBytes);
+}
+
 int plan_mlp(int64_t T, int64_t D, int64_t H, int64_t Dout, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
+  if (fused_small(T, D, H, Dout, true)) return FMLP_PLAN_FUSED_SMALL;
+  if (decode_ok(T, D, H, Dout, 1, sms)) return FMLP_PLAN_DECODE;
   if (gemv_ok(T, D, H, 1, sms) && gemv_ok(T, H, Dout, 1, sms) &&
       gemv_preferred(T, mat_bytes(H, D) + mat_bytes(Dout, H)))
     return FMLP_PLAN_GEMV;
   return FMLP_PLAN_TC;
 }
 
-// The fused single-kernel plan depends on the shape alone (never on the SM count), so the
-// workspace query and the call always agree on whether m needs a workspace.
 int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
-  const bool gemv_shape = T <= kGemvMaxT && D % 256 == 0 && H % 256 == 0;
-  if (gemv_shape) {
-    if (gemv_ok(T, D, H, 2, sms) && gemv_ok(T, H, D, 1, sms) &&
-        gemv_preferred(T, 3 * mat_bytes(H, D)))
-      return FMLP_PLAN_GEMV;
-    return FMLP_PLAN_TC;
-  }
-  if (D <= kSmallMaxD && D % 16 == 0 && H <= kSmallMaxH) return FMLP_PLAN_FUSED_SMALL;
+  if (fused_small(T, D, H, D, false)) return FMLP_PLAN_FUSED_SMALL;
+  if (decode_ok(T, D, H, D, 2, sms)) return FMLP_PLAN_DECODE;
+  if (T <= kGemvMaxT && D % 256 == 0 && H % 256 == 0 && gemv_ok(T, D, H, 2, sms) &&
+      gemv_ok(T, H, D, 1, sms) && gemv_preferred(T, 3 * mat_bytes(H, D)))
+    return FMLP_PLAN_GEMV;
   return FMLP_PLAN_TC;
 }
 
@@ -467,6 +601,7 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
                         const void* W1, const void* bias, void* y, int64_t T, int64_t K,
                         int64_t N, int gelu_mode, cudaStream_t s, int64_t ldx = 0,
                         int64_t ldy = 0) {
+  FMLP_LAUNCH_GUARD("gemv launch");
   GemvLaunch L;
   L.x = x;
   L.W0 = W0;
@@ -488,19 +623,32 @@ fmlp_status launch_gemv(const DeviceState& d, int epi, const void* x, const void
   return FMLP_OK;
 }
 
-fmlp_status launch_small(const DeviceState& d, const void* x, const void* Wg, const void* Wu,
-                         const void* Wd, void* y, int64_t T, int64_t D, int64_t H,
-                         cudaStream_t s) {
+// The whole block in one kernel (small D and Dout). GeGLU: W1 = Wg, Wu, W2 = Wd, Dout = D,
+// no biases. MLP: W1, W2 with nullable biases b1, b2 and the activation `mode`.
+fmlp_status launch_small(const DeviceState& d, bool mlp, const void* x, const void* W1,
+                         const void* Wu, const void* W2, const void* b1, const void* b2, void* y,
+                         int64_t T, int64_t D, int64_t H, int64_t Dout, int mode,
+                         cudaStream_t s, int64_t ldx = 0, int64_t ldy = 0) {
+  FMLP_LAUNCH_GUARD("fused small launch");
   SmallLaunch L;
   memset(&L, 0, sizeof L);
-  FMLP_TRY(make_map(&L.tmX, x, T, D, 128, "x"));
-  FMLP_TRY(make_map(&L.tmWg, Wg, H, D, 64, "Wg"));
-  FMLP_TRY(make_map(&L.tmWu, Wu, H, D, 64, "Wu"));
-  FMLP_TRY(make_map(&L.tmWd, Wd, D, H, static_cast<uint32_t>(D), "Wd"));
-  FMLP_TRY(make_map(&L.tmY, y, T, D, 32, "y"));
+  FMLP_TRY(make_map(&L.tmX, x, T, D, 128, "x", ldx));
+  FMLP_TRY(make_map(&L.tmWg, W1, H, D, 64, mlp ? "W1" : "Wg"));
+  if (mlp) {
+    L.tmWu = L.tmWg;
+  } else {
+    FMLP_TRY(make_map(&L.tmWu, Wu, H, D, 64, "Wu"));
+  }
+  FMLP_TRY(make_map(&L.tmWd, W2, Dout, H, static_cast<uint32_t>(Dout), mlp ? "W2" : "Wd"));
+  FMLP_TRY(make_map(&L.tmY, y, T, Dout, 32, "y", ldy));
+  L.b1 = b1;
+  L.b2 = b2;
   L.T = static_cast<int>(T);
   L.D = static_cast<int>(D);
   L.H = static_cast<int>(H);
+  L.Dout = static_cast<int>(Dout);
+  L.mlp = mlp;
+  L.gelu_mode = mode;
   L.status = d.status;
   L.timeout_ns = kWaitTimeoutNs;
   L.stream = s;
@@ -509,7 +657,67 @@ fmlp_status launch_small(const DeviceState& d, const void* x, const void* Wg, co
   return FMLP_OK;
 }
 
+// One-kernel decode of the whole block. Falls back (returns FMLP_PLAN_NONE in *ran = false)
+// when this device cannot run it or every grid-barrier counter is taken.
+fmlp_status launch_decode(DeviceState& d, bool geglu, const void* x, const void* W1a,
+                          const void* W1b, const void* b1, const void* W2, const void* b2,
+                          void* h, void* y, int64_t T, int64_t D, int64_t H, int64_t Dout,
+                          int gelu_mode, cudaStream_t s, bool* ran, int64_t ldx, int64_t ldy) {
+  *ran = false;
+  if (d.decode_occ < 1 || !d.decode_bar) return FMLP_OK;
+  int slot = -1;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < d.decode_streams; ++i)
+      if (d.decode_stream[i] == s) {
+        slot = i;
+        break;
+      }
+    if (slot < 0 && d.decode_streams < kDecodeSlots) {
+      slot = d.decode_streams++;
+      d.decode_stream[slot] = s;
+    }
+  }
+  if (slot < 0) return FMLP_OK;
+  FMLP_LAUNCH_GUARD("decode launch");
+  DecodeLaunch L;
+  memset(&L, 0, sizeof L);
+  L.x = x;
+  L.W1a = W1a;
+  L.W1b = W1b;
+  L.b1 = b1;
+  L.W2 = W2;
+  L.b2 = b2;
+  L.h = h;
+  L.y = y;
+  L.T = static_cast<int>(T);
+  L.D = static_cast<int>(D);
+  L.H = static_cast<int>(H);
+  L.Dout = static_cast<int>(Dout);
+  L.ldx = static_cast<int>(ldx);
+  L.ldy = static_cast<int>(ldy);
+  L.geglu = geglu;
+  L.gelu_mode = gelu_mode;
+  L.grid = d.sms * std::min(d.decode_occ, 1) + g_decode_extra_ctas.load(std::memory_order_relaxed);
+  L.barrier = d.decode_bar + 16 * slot;
+  L.status = d.status;
+  const unsigned long long tmo = g_decode_timeout_ns.load(std::memory_order_relaxed);
+  L.timeout_ns = tmo ? tmo : kWaitTimeoutNs;
+  L.stream = s;
+  const cudaError_t e = decode_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  *ran = true;
+  return FMLP_OK;
+}
+
 }  // namespace
+
+int validate_block_dims(int64_t T, int64_t D, int64_t H) {
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(D, "D"));
+  FMLP_TRY(check_inner(H, "H"));
+  return FMLP_OK;
+}
 
 void record_error(const char* fmt, ...) {
   char buf[512];
@@ -545,24 +753,46 @@ const char* fmlp_status_string(fmlp_status st) {
 
 const char* fmlp_last_error(void) { return t_last_error.c_str(); }
 
+// Every plan but the single-kernel small GeGLU keeps the intermediate (T x H bf16) in the
+// workspace, so the size depends on the shape alone.
 size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
-  const int p = plan_geglu(T, D, H, kPlanSms);
-  return (p == FMLP_PLAN_TC || p == FMLP_PLAN_GEMV) ? mat_bytes(T, H) : 0;
+  if (T <= 0 || H <= 0) return 0;
+  return plan_geglu(T, D, H, plan_sms()) == FMLP_PLAN_FUSED_SMALL ? 0 : mat_bytes(T, H);
 }
 
 size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout) {
-  if (plan_mlp(T, D, H, Dout, kPlanSms) == FMLP_PLAN_NONE) return 0;
-  return mat_bytes(T, H);
+  if (T <= 0 || H <= 0) return 0;
+  return plan_mlp(T, D, H, Dout, plan_sms()) == FMLP_PLAN_FUSED_SMALL ? 0 : mat_bytes(T, H);
 }
 
-int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) { return plan_geglu(T, D, H, kPlanSms); }
+int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) { return plan_geglu(T, D, H, plan_sms()); }
 
 int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout) {
-  return plan_mlp(T, D, H, Dout, kPlanSms);
+  return plan_mlp(T, D, H, Dout, plan_sms());
 }
 
 int fmlp_linear_plan(int64_t T, int64_t in, int64_t out) {
-  return plan_linear(T, in, out, kPlanSms);
+  return plan_linear(T, in, out, plan_sms());
+}
+
+// Row strides of x [T, in] and y [T, out] in elements: 0 means packed rows (the stride is
+// the row length); otherwise at least the row length (else FMLP_ERR_SHAPE) and a multiple of
+// 8, the 16-byte row rule of the TMA loads and stores (else FMLP_ERR_ALIGN).
+static fmlp_status resolve_strides(int64_t* ldx, int64_t* ldy, int64_t in, int64_t out) {
+  if (*ldx == 0) *ldx = in;
+  if (*ldy == 0) *ldy = out;
+  if (*ldx < in || *ldy < out || *ldx > kMaxDim || *ldy > kMaxDim) {
+    set_error("row strides ldx = %lld, ldy = %lld must be at least the rows' lengths %lld, %lld",
+              static_cast<long long>(*ldx), static_cast<long long>(*ldy),
+              static_cast<long long>(in), static_cast<long long>(out));
+    return FMLP_ERR_SHAPE;
+  }
+  if (*ldx % 8 != 0 || *ldy % 8 != 0) {
+    set_error("row strides ldx = %lld, ldy = %lld are not multiples of 8 elements (16 bytes)",
+              static_cast<long long>(*ldx), static_cast<long long>(*ldy));
+    return FMLP_ERR_ALIGN;
+  }
+  return FMLP_OK;
 }
 
 // ldx, ldy: row strides of x and y in elements (0: packed rows).
@@ -573,19 +803,7 @@ static fmlp_status linear_common(const void* x, const void* W, const void* b, vo
   FMLP_TRY(check_T(T));
   FMLP_TRY(check_inner(in, "in"));
   FMLP_TRY(check_inner(out, "out"));
-  if (ldx == 0) ldx = in;
-  if (ldy == 0) ldy = out;
-  if (ldx < in || ldy < out || ldx > kMaxDim || ldy > kMaxDim) {
-    set_error("row strides ldx = %lld, ldy = %lld must be at least in = %lld, out = %lld",
-              static_cast<long long>(ldx), static_cast<long long>(ldy),
-              static_cast<long long>(in), static_cast<long long>(out));
-    return FMLP_ERR_SHAPE;
-  }
-  if (ldx % 8 != 0 || ldy % 8 != 0) {
-    set_error("row strides ldx = %lld, ldy = %lld are not multiples of 8 elements (16 bytes)",
-              static_cast<long long>(ldx), static_cast<long long>(ldy));
-    return FMLP_ERR_ALIGN;
-  }
+  FMLP_TRY(resolve_strides(&ldx, &ldy, in, out));
   if (epi == EPI_BIAS_GELU && !act_mode_ok(mode)) {
     set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU", mode);
     return FMLP_ERR_SHAPE;
@@ -651,13 +869,15 @@ fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, vo
   return launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
 }
 
-fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
-                       int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
-                       fmlp_stream_t s) {
+// ldx, ldy: row strides of x and y in elements (0: packed rows).
+static fmlp_status geglu_common(const void* x, int64_t ldx, const void* Wg, const void* Wu,
+                                const void* Wd, void* y, int64_t ldy, int64_t T, int64_t D,
+                                int64_t H, void* ws, size_t ws_bytes, fmlp_stream_t s) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
+  FMLP_TRY(resolve_strides(&ldx, &ldy, D, D));
   if (T == 0) return FMLP_OK;
   FMLP_NONNULL(x, "x");
   FMLP_NONNULL(Wg, "Wg");
@@ -669,9 +889,9 @@ fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void
     set_error("workspace has %zu bytes, needs %zu", ws_bytes, need);
     return FMLP_ERR_WORKSPACE;
   }
-  const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, mat_bytes(H, D), "Wg"},
-      ru{Wu, mat_bytes(H, D), "Wu"}, rd{Wd, mat_bytes(D, H), "Wd"}, ry{y, mat_bytes(T, D), "y"},
-      rw{ws, ws ? need : 0, "workspace"};
+  const Range rx{x, mat_bytes(1, D), "x", T, mat_bytes(1, ldx)}, rg{Wg, mat_bytes(H, D), "Wg"},
+      ru{Wu, mat_bytes(H, D), "Wu"}, rd{Wd, mat_bytes(D, H), "Wd"},
+      ry{y, mat_bytes(1, D), "y", T, mat_bytes(1, ldy)}, rw{ws, ws ? need : 0, "workspace"};
   const Range all[6] = {rx, rg, ru, rd, ry, rw};
   FMLP_TRY(check_ptrs(all, 6));
   const Range ins_y[5] = {rx, rg, ru, rd, rw};
@@ -682,26 +902,48 @@ fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void
   FMLP_TRY(device_state(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   const int plan = plan_geglu(T, D, H, d->sms);
-  if (plan == FMLP_PLAN_FUSED_SMALL) return launch_small(*d, x, Wg, Wu, Wd, y, T, D, H, st);
+  if (plan == FMLP_PLAN_FUSED_SMALL)
+    return launch_small(*d, false, x, Wg, Wu, Wd, nullptr, nullptr, y, T, D, H, D, 0, st, ldx,
+                        ldy);
   void* m = ws;
   if (!m) {
     cudaError_t e = cudaMallocAsync(&m, need, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
   }
-  fmlp_status r;
-  if (plan == FMLP_PLAN_GEMV) {
-    r = launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st);
-    if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st);
-  } else {
-    r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st);
+  fmlp_status r = FMLP_OK;
+  bool ran = false;
+  if (plan == FMLP_PLAN_DECODE)
+    r = launch_decode(*d, true, x, Wg, Wu, nullptr, Wd, nullptr, m, y, T, D, H, D, 0, st, &ran,
+                      ldx, ldy);
+  if (ran || r != FMLP_OK) {
+    // done (or failed) in one kernel
+  } else if (plan == FMLP_PLAN_GEMV || (plan == FMLP_PLAN_DECODE && gemv_ok(T, D, H, 2, d->sms) &&
+                                        gemv_ok(T, H, D, 1, d->sms))) {
+    r = launch_gemv(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, D, H, 0, st, ldx, 0);
     if (r == FMLP_OK)
-      r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st);
+      r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st, 0, ldy);
+  } else {
+    r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st, ldx, 0);
+    if (r == FMLP_OK)
+      r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st, 0, ldy);
   }
   if (!ws) {
     cudaError_t e = cudaFreeAsync(m, st);
     if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
   }
   return r;
+}
+
+fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
+                       int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
+                       fmlp_stream_t s) {
+  return geglu_common(x, 0, Wg, Wu, Wd, y, 0, T, D, H, ws, ws_bytes, s);
+}
+
+fmlp_status fmlp_geglu_strided(const void* x, int64_t ldx, const void* Wg, const void* Wu,
+                               const void* Wd, void* y, int64_t ldy, int64_t T, int64_t D,
+                               int64_t H, void* ws, size_t ws_bytes, fmlp_stream_t s) {
+  return geglu_common(x, ldx, Wg, Wu, Wd, y, ldy, T, D, H, ws, ws_bytes, s);
 }
 
 size_t fmlp_moe_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
@@ -789,6 +1031,11 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
     L.groups = static_cast<int>(E);
     L.ydir = gu ? m : y;
     L.ldy = static_cast<int>(N);
+    if (take_injection(g_inject_launch)) {
+      set_error("grouped gemm launch: injected launch failure (fmlp_test_inject)");
+      r = FMLP_ERR_CUDA;
+      break;
+    }
     const cudaError_t e = pair ? gemm_tc2_grouped_launch(L) : gemm_tc_grouped_launch(L);
     if (e != cudaSuccess) r = cuda_fail(e, "grouped gemm launch");
   }
@@ -799,14 +1046,17 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
   return r;
 }
 
-fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const void* W2,
-                          const void* b2, void* y, int64_t T, int64_t D, int64_t H, int64_t Dout,
-                          fmlp_gelu_mode mode, void* ws, size_t ws_bytes, fmlp_stream_t s) {
+// ldx, ldy: row strides of x and y in elements (0: packed rows).
+static fmlp_status mlp_common(const void* x, int64_t ldx, const void* W1, const void* b1,
+                              const void* W2, const void* b2, void* y, int64_t ldy, int64_t T,
+                              int64_t D, int64_t H, int64_t Dout, fmlp_gelu_mode mode, void* ws,
+                              size_t ws_bytes, fmlp_stream_t s) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
   FMLP_TRY(check_inner(Dout, "Dout"));
+  FMLP_TRY(resolve_strides(&ldx, &ldy, D, Dout));
   if (!act_mode_ok(mode)) {
     set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU",
               static_cast<int>(mode));
@@ -822,10 +1072,10 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
     set_error("workspace has %zu bytes, needs %zu", ws_bytes, need);
     return FMLP_ERR_WORKSPACE;
   }
-  const Range rx{x, mat_bytes(T, D), "x"}, r1{W1, mat_bytes(H, D), "W1"},
+  const Range rx{x, mat_bytes(1, D), "x", T, mat_bytes(1, ldx)}, r1{W1, mat_bytes(H, D), "W1"},
       rb1{b1, b1 ? mat_bytes(1, H) : 0, "b1"}, r2{W2, mat_bytes(Dout, H), "W2"},
-      rb2{b2, b2 ? mat_bytes(1, Dout) : 0, "b2"}, ry{y, mat_bytes(T, Dout), "y"},
-      rw{ws, ws ? need : 0, "workspace"};
+      rb2{b2, b2 ? mat_bytes(1, Dout) : 0, "b2"},
+      ry{y, mat_bytes(1, Dout), "y", T, mat_bytes(1, ldy)}, rw{ws, ws ? need : 0, "workspace"};
   const Range all[7] = {rx, r1, rb1, r2, rb2, ry, rw};
   FMLP_TRY(check_ptrs(all, 7));
   const Range ins_y[6] = {rx, r1, rb1, r2, rb2, rw};
@@ -835,27 +1085,54 @@ fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const v
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int plan = plan_mlp(T, D, H, Dout, d->sms);
+  if (plan == FMLP_PLAN_FUSED_SMALL)
+    return launch_small(*d, true, x, W1, nullptr, W2, b1, b2, y, T, D, H, Dout,
+                        static_cast<int>(mode), st, ldx, ldy);
   void* h = ws;
   if (!h) {
     cudaError_t e = cudaMallocAsync(&h, need, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
   }
-  fmlp_status r;
-  if (plan_mlp(T, D, H, Dout, d->sms) == FMLP_PLAN_GEMV) {
+  fmlp_status r = FMLP_OK;
+  bool ran = false;
+  if (plan == FMLP_PLAN_DECODE)
+    r = launch_decode(*d, false, x, W1, nullptr, b1, W2, b2, h, y, T, D, H, Dout,
+                      static_cast<int>(mode), st, &ran, ldx, ldy);
+  if (ran || r != FMLP_OK) {
+    // done (or failed) in one kernel
+  } else if (plan == FMLP_PLAN_GEMV ||
+             (plan == FMLP_PLAN_DECODE && gemv_ok(T, D, H, 1, d->sms) &&
+              gemv_ok(T, H, Dout, 1, d->sms))) {
     r = launch_gemv(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, D, H, static_cast<int>(mode),
-                    st);
-    if (r == FMLP_OK) r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st);
+                    st, ldx, 0);
+    if (r == FMLP_OK)
+      r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st, 0, ldy);
   } else {
     r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D, static_cast<int>(mode),
-                    false, st);
+                    false, st, ldx, 0);
     if (r == FMLP_OK)
-      r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st);
+      r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st, 0, ldy);
   }
   if (!ws) {
     cudaError_t e = cudaFreeAsync(h, st);
     if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(workspace)");
   }
   return r;
+}
+
+fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1, const void* W2,
+                          const void* b2, void* y, int64_t T, int64_t D, int64_t H, int64_t Dout,
+                          fmlp_gelu_mode mode, void* ws, size_t ws_bytes, fmlp_stream_t s) {
+  return mlp_common(x, 0, W1, b1, W2, b2, y, 0, T, D, H, Dout, mode, ws, ws_bytes, s);
+}
+
+fmlp_status fmlp_mlp_gelu_strided(const void* x, int64_t ldx, const void* W1, const void* b1,
+                                  const void* W2, const void* b2, void* y, int64_t ldy,
+                                  int64_t T, int64_t D, int64_t H, int64_t Dout,
+                                  fmlp_gelu_mode mode, void* ws, size_t ws_bytes,
+                                  fmlp_stream_t s) {
+  return mlp_common(x, ldx, W1, b1, W2, b2, y, ldy, T, D, H, Dout, mode, ws, ws_bytes, s);
 }
 
 static std::string describe_gemm(const DeviceState& d, const char* name, int epi, int64_t M,
@@ -893,6 +1170,19 @@ static std::string describe_gemv(const DeviceState& d, const char* name, int64_t
   return b;
 }
 
+static std::string describe_decode(const DeviceState& d, const char* name, int64_t T, int64_t D,
+                                   int64_t H, int64_t Dout, int nmat) {
+  char b[256];
+  snprintf(b, sizeof b,
+           "%s: one weight-streaming kernel for both layers (grid barrier between them), "
+           "T=%lld D=%lld H=%lld Dout=%lld, grid=%d, shared memory per CTA=%zu bytes",
+           name, static_cast<long long>(T), static_cast<long long>(D), static_cast<long long>(H),
+           static_cast<long long>(Dout), d.sms,
+           decode_smem_bytes(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
+                             static_cast<int>(Dout), nmat, d.sms));
+  return b;
+}
+
 fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t Dout, char* buf,
                                size_t buflen) {
   t_last_error.clear();
@@ -916,7 +1206,9 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
                                     : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
   } else if (op == 3) {              // geglu block
     const int p = plan_geglu(T, D, H, d->sms);
-    if (p == FMLP_PLAN_FUSED_SMALL) {
+    if (p == FMLP_PLAN_DECODE) {
+      r = describe_decode(*d, "GeGLU block", T, D, H, D, 2);
+    } else if (p == FMLP_PLAN_FUSED_SMALL) {
       char b[160];
       snprintf(b, sizeof b, "fused block: one kernel, grid=%lld", static_cast<long long>((T + 127) / 128));
       r = b;
@@ -927,7 +1219,15 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
           describe_gemm(*d, "down", EPI_BIAS, T, D, H);
     }
   } else if (op == 4) {              // mlp: D -> H -> Dout
-    if (plan_mlp(T, D, H, Dout, d->sms) == FMLP_PLAN_GEMV)
+    const int p = plan_mlp(T, D, H, Dout, d->sms);
+    if (p == FMLP_PLAN_FUSED_SMALL) {
+      char b[160];
+      snprintf(b, sizeof b, "fused block: one kernel, grid=%lld",
+               static_cast<long long>((T + 127) / 128));
+      r = b;
+    } else if (p == FMLP_PLAN_DECODE)
+      r = describe_decode(*d, "MLP block", T, D, H, Dout, 1);
+    else if (p == FMLP_PLAN_GEMV)
       r = describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
     else
       r = describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
@@ -987,11 +1287,51 @@ fmlp_status fmlp_device_status(fmlp_stream_t s) {
 
   static const char* sites[] = {"?",          "test wait",          "producer (empty slot)",
                                 "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
-                                "drain",      "fused kernel", "GEMV"};
+                                "drain",      "fused kernel", "GEMV",
+                                "decode (layer-2 weight copy)", "decode (grid barrier)"};
   const int site = v >> 8;
   set_error("a kernel gave up waiting at: %s (code 0x%x)",
-            (site >= 0 && site < 9) ? sites[site] : "?", v);
+            (site >= 0 && site < 11) ? sites[site] : "?", v);
   return static_cast<fmlp_status>(v & 0xFF);
+}
+
+fmlp_status fmlp_test_inject(int kind, int64_t count, int64_t timeout_us) {
+  t_last_error.clear();
+  if (count < 0 || count > 1000000 || timeout_us < 0 || timeout_us > 2000000) {
+    set_error("count = %lld (0..1000000) or timeout_us = %lld (0..2000000) out of range",
+              static_cast<long long>(count), static_cast<long long>(timeout_us));
+    return FMLP_ERR_SHAPE;
+  }
+  switch (kind) {
+    case FMLP_INJECT_NONE:
+      g_inject_launch.store(0);
+      g_inject_skip.store(0);
+      g_inject_timeout_ns.store(0);
+      return FMLP_OK;
+    case FMLP_INJECT_LAUNCH:
+      g_inject_launch.store(static_cast<int>(count));
+      return FMLP_OK;
+    case FMLP_INJECT_SKIP_LOAD:
+      g_inject_timeout_ns.store(static_cast<unsigned long long>(timeout_us) * 1000ull);
+      g_inject_skip.store(static_cast<int>(count));
+      return FMLP_OK;
+    default:
+      set_error("injection kind %d unknown", kind);
+      return FMLP_ERR_SHAPE;
+  }
+}
+
+fmlp_status fmlp_test_decode_overload(int64_t extra_ctas, int64_t timeout_us) {
+  t_last_error.clear();
+  if (extra_ctas < 0 || extra_ctas > 4096 || timeout_us < 0 || timeout_us > 2000000) {
+    set_error("extra_ctas = %lld (0..4096) or timeout_us = %lld (0..2000000) out of range",
+              static_cast<long long>(extra_ctas), static_cast<long long>(timeout_us));
+    return FMLP_ERR_SHAPE;
+  }
+  g_decode_extra_ctas.store(static_cast<int>(extra_ctas), std::memory_order_relaxed);
+  g_decode_timeout_ns.store(static_cast<unsigned long long>(timeout_us) * 1000ull,
+                            std::memory_order_relaxed);
+  return FMLP_OK;
 }
 
 fmlp_status fmlp_test_wait_timeout(int64_t timeout_us, fmlp_stream_t s) {

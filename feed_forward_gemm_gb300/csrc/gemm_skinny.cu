@@ -36,10 +36,21 @@ constexpr int kSkBK = 64;                   // K per stage: one 128-byte swizzle
 constexpr int kSkRows = 128;                // weight rows per tile (MMA M)
 constexpr int kSkA = kSkRows * kSkBK * 2;   // 16 KB of weights per matrix per stage
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
   return v;
+}
+
+template <int EPI>
+__device__ __forceinline__ float skinny_out(float a0, float a1, const __nv_bfloat16* bias, int n,
+                                            int gelu_mode) {
+  if (EPI == EPI_GEGLU) return gelu_tanh_f(a0) * a1;
+  const float z = a0 + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
+  return EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
 }
 
 }  // namespace
@@ -171,33 +182,58 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   cluster_sync();   // every slice of the tile is in its CTA's shared memory
 
   // ------------------------------------------------------------------ cluster reduction
-  // CTA s finishes rows [s * rr, (s + 1) * rr) of the tile for every token: consecutive
-  // threads take consecutive rows, so the writes of y[t, n0 + row] are contiguous.
+  // CTA s finishes rows [s * rr, (s + 1) * rr) of the tile for every token, four consecutive
+  // rows per thread: all S slices of the four rows (16-byte distributed-shared-memory loads,
+  // every slice in flight at once) are added in slice order q = 0..S-1, the same order for
+  // every element and every run. Consecutive threads take consecutive row groups, so the
+  // writes of y[t, n0 + row .. + 3] are contiguous 8-byte stores.
   {
     const int rr = kSkRows / S;
+    const int rg = rr / 4;
     const uint32_t part_addr = smem_u32(part);
-    for (int e = threadIdx.x; e < rr * T; e += kSkThreads) {
-      const int t = e / rr;
-      const int row = s * rr + (e - t * rr);
+    for (int e = threadIdx.x; e < rg * T; e += kSkThreads) {
+      const int t = e / rg;
+      const int row = s * rr + (e - t * rg) * 4;
       const int n = n0 + row;
       if (n >= N) continue;
-      float acc[NMAT];
+      float4 q4[NMAT][8];
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
-        const uint32_t off =
-            static_cast<uint32_t>(((mat * Tpad + t) * kSkRows + row) * static_cast<int>(sizeof(float)));
-        float v = 0.f;
-        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(mapa_shared(part_addr + off, static_cast<uint32_t>(q)));
-        acc[mat] = v;
+        const uint32_t off = static_cast<uint32_t>(((mat * Tpad + t) * kSkRows + row) *
+                                                   static_cast<int>(sizeof(float)));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < S) q4[mat][q] = ld_dsmem_v4(mapa_shared(part_addr + off, static_cast<uint32_t>(q)));
       }
-      float out;
-      if (EPI == EPI_GEGLU) {
-        out = gelu_tanh_f(acc[0]) * acc[NMAT - 1];
+      float4 acc[NMAT];
+#pragma unroll
+      for (int mat = 0; mat < NMAT; ++mat) {
+        acc[mat] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < S) {
+            acc[mat].x += q4[mat][q].x;
+            acc[mat].y += q4[mat][q].y;
+            acc[mat].z += q4[mat][q].z;
+            acc[mat].w += q4[mat][q].w;
+          }
+        }
+      }
+      const float o0 = skinny_out<EPI>(acc[0].x, acc[NMAT - 1].x, bias, n, gelu_mode);
+      const float o1 = skinny_out<EPI>(acc[0].y, acc[NMAT - 1].y, bias, n + 1, gelu_mode);
+      const float o2 = skinny_out<EPI>(acc[0].z, acc[NMAT - 1].z, bias, n + 2, gelu_mode);
+      const float o3 = skinny_out<EPI>(acc[0].w, acc[NMAT - 1].w, bias, n + 3, gelu_mode);
+      __nv_bfloat16* yr = y + static_cast<size_t>(t) * ldy + n;
+      if (n + 3 < N) {
+        uint2 pk;
+        pk.x = pack_bf16x2(o0, o1);
+        pk.y = pack_bf16x2(o2, o3);
+        *reinterpret_cast<uint2*>(yr) = pk;
       } else {
-        const float z = acc[0] + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
-        out = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
+        yr[0] = __float2bfloat16_rn(o0);
+        if (n + 1 < N) yr[1] = __float2bfloat16_rn(o1);
+        if (n + 2 < N) yr[2] = __float2bfloat16_rn(o2);
       }
-      y[static_cast<size_t>(t) * ldy + n] = __float2bfloat16_rn(out);
     }
   }
   cluster_sync();   // no CTA leaves while another may still read its shared memory

@@ -18,7 +18,9 @@
 //   tfull[b]   (both CTAs) accumulator b ready, multicast commit.
 //   tempty[b]  (even CTA) 256 arrivals: every epilogue thread of both CTAs.
 // Cluster barriers bracket the kernel so neither CTA leaves while the other may still touch
-// its shared memory or TMEM. Every mbarrier wait is bounded.
+// its shared memory or TMEM. Every mbarrier wait is bounded: a wait that runs out records the
+// site and ends its role's loop; the MMA thread drains its commits, the even CTA's producer
+// waits (bounded) for the loads it issued, and every thread reaches the final cluster barrier.
 //
 // GROUPED (mixture of experts): as in the single-SM kernel, the rows of A are grouped by expert
 // with the E + 1 offsets read on the device, each group's tiles walk 256-row tile fastest, each CTA
@@ -90,7 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     const __nv_bfloat16* __restrict__ bias, int M, int N_out, int K,
                     int gelu_mode, int group, int* status, uint64_t timeout_ns,
                     const int* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ ydir,
-                    int ldy) {
+                    int ldy, int skip_first_load) {
   using C = PairCfg<BN>;
   constexpr int kPairStages = C::STAGES;
   constexpr int kPairStage = C::STAGE;
@@ -197,6 +199,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           uint8_t* sA = stages + stage * kPairStage;
           uint8_t* sB = sA + kPairA;
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
+          // test hook: the first K step of the pair's first tile expects its bytes but no load
+          // brings them, so the MMA's bounded wait on this stage runs out
+          if (skip_first_load && t == pair && kb == 0) {
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           const uint32_t fb = full0 + static_cast<uint32_t>(stage * 8);
           tma_load_2d_pair(sA, &tmA, fb, kb * kPairBK, a_row);
           if constexpr (GROUPED)
@@ -328,7 +339,7 @@ static cudaError_t launch_pair(const GemmLaunch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB0, L.tmB1, L.tmY,
                             static_cast<const __nv_bfloat16*>(L.bias), L.M, L.N_out, L.K,
                             L.gelu_mode, group, L.status, L.timeout_ns, L.offsets, L.groups,
-                            static_cast<__nv_bfloat16*>(L.ydir), L.ldy);
+                            static_cast<__nv_bfloat16*>(L.ydir), L.ldy, L.skip_first_load ? 1 : 0);
 }
 
 cudaError_t gemm_tc2_launch(const GemmLaunch& L) {

@@ -62,6 +62,8 @@ struct GemmLaunch {
   int groups;
   void* ydir;
   int ldy;
+  // Test hook (CTA-pair kernel): skip the loads of the first K step (see fmlp_test_inject).
+  bool skip_first_load;
 };
 constexpr int kMoeMaxExperts = 256;
 
@@ -118,25 +120,66 @@ int gemv_grid(int T, int K, int N, int nmat, int sms);
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);
 cudaError_t gemv_launch(const GemvLaunch& L);
 
-// Whole GeGLU block in one kernel for small D (fused plan).
-constexpr int kSmallMaxD = 256;
-constexpr int kSmallMaxH = 2048;
-struct SmallLaunch {
-  CUtensorMap tmX;    // x  [T, D], box {64, 128}
-  CUtensorMap tmWg;   // Wg [H, D], box {64, 64}
-  CUtensorMap tmWu;   // Wu [H, D], box {64, 64}
-  CUtensorMap tmWd;   // Wd [D, H], box {64, D}
-  CUtensorMap tmY;    // y  [T, D], box {64, 32}
-  int T, D, H;
+// The whole block (both layers) in one weight-streaming kernel for 1..kDecodeMaxT tokens
+// (decode.cu): one CTA per SM, every CTA resident, a bounded grid barrier between the layers.
+constexpr int kDecodeMaxT = 4;
+constexpr int kDecodeSlots = 1024;           // grid-barrier counters per device
+constexpr size_t kDecodeMaxSmem = 232448;    // 227 KB: the opt-in shared memory of one CTA
+struct DecodeLaunch {
+  const void* x;      // [T, D], row stride ldx
+  const void* W1a;    // [H, D]  W1 (MLP) or Wg (GeGLU)
+  const void* W1b;    // [H, D]  Wu (GeGLU), else nullptr
+  const void* b1;     // [H] or nullptr (MLP)
+  const void* W2;     // [Dout, H]
+  const void* b2;     // [Dout] or nullptr
+  void* h;            // [T, H] workspace (the layer-1 output)
+  void* y;            // [T, Dout], row stride ldy
+  int T, D, H, Dout;
+  int ldx, ldy;
+  bool geglu;
+  int gelu_mode;
+  int grid;           // CTAs; all must be resident at once
+  unsigned long long* barrier;   // this launch's grid-barrier counter
   int* status;
   uint64_t timeout_ns;
   cudaStream_t stream;
 };
-int ffn_small_smem_bytes(int D);
+// Dynamic shared memory the decode kernel needs for these sizes on `grid` CTAs (the token
+// vectors and the per-warp row sums); the plan requires it to fit in kDecodeMaxSmem.
+size_t decode_smem_bytes(int T, int D, int H, int Dout, int nmat, int grid);
+cudaError_t decode_launch(const DecodeLaunch& L);
+// Device address of the first grid-barrier counter (slot i is at + 16 * i).
+cudaError_t decode_barrier_base(unsigned long long** p);
+// Resident CTAs per SM of the decode kernel at its largest shared memory (0: it cannot run).
+cudaError_t decode_occupancy(int* per_sm);
+
+// Whole block in one kernel for small D and Dout (fused plan): the GeGLU block, or
+// Linear -> act -> Linear with biases.
+constexpr int kSmallMaxD = 256;
+constexpr int kSmallMaxH = 2048;
+struct SmallLaunch {
+  CUtensorMap tmX;    // x  [T, D], box {64, 128}
+  CUtensorMap tmWg;   // Wg or W1 [H, D], box {64, 64}
+  CUtensorMap tmWu;   // Wu [H, D], box {64, 64} (GeGLU only)
+  CUtensorMap tmWd;   // Wd or W2 [Dout, H], box {64, Dout}
+  CUtensorMap tmY;    // y  [T, Dout], box {64, 32}
+  const void* b1;     // [H] or nullptr (MLP only)
+  const void* b2;     // [Dout] or nullptr (MLP only)
+  int T, D, H, Dout;
+  bool mlp;           // Linear -> act -> Linear (else GeGLU, Dout == D)
+  int gelu_mode;
+  int* status;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+int ffn_small_smem_bytes(int D, int Dout);
 cudaError_t ffn_small_launch(const SmallLaunch& L);
 
 // Records the calling thread's fmlp_last_error() text (printf-style).
 void record_error(const char* fmt, ...);
+
+// The shape checks every block call starts with (T, then D, then H), as an fmlp_status value.
+int validate_block_dims(int64_t T, int64_t D, int64_t H);
 
 // Device GELU check kernel.
 cudaError_t gelu_eval_launch(const float* in, float* out, int64_t n, int mode,

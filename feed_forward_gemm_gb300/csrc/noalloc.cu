@@ -1,18 +1,18 @@
 // fmlp_geglu_noalloc: the GeGLU block for callers that must not allocate device memory.
 //
 // Some callers cannot call cudaMalloc or any allocating routine: a plugin inside a serving
-// process whose memory pool owns the whole device and forbids allocations after start-up, a
-// real-time loop that may not risk an allocation stall or failure, or code that records
-// work into a CUDA graph where an allocation would break the capture. fmlp_geglu needs a
-// workspace for the intermediate m between its two kernels; this entry point takes that
-// workspace from a fixed array in the library's own device memory instead, so it allocates
-// nothing.
+// process whose memory pool owns the whole device and forbids allocations after start-up, or
+// a real-time loop that may not risk an allocation stall or failure. fmlp_geglu needs a
+// workspace for the intermediate m between its stages; this entry point takes that workspace
+// from a fixed array in the library's own device memory instead, so it allocates nothing.
 //
 // The array lives at file scope as a static __device__ object, so every GPU that loads the
 // library holds it until the process exits. In host code its name is only a host-side stand-
 // in, never a device address: the address kernels use is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and cached. The first call on a device does
-// that look-up; make it before any stream capture on that device.
+// that look-up; make it before any stream capture on that device. A device reset
+// (cudaDeviceReset) while the library is loaded leaves the cached address stale and is not
+// supported.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,7 +25,7 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 
-// Holds m (T x H bf16) between the gate/up and down kernels; shared by every call.
+// Holds m (T x H bf16) between the GeGLU block's stages; shared by every call.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
@@ -39,6 +39,9 @@ using namespace fmlp;
 extern "C" fmlp_status fmlp_geglu_noalloc(const void* x, const void* Wg, const void* Wu,
                                           const void* Wd, void* y, int64_t T, int64_t D,
                                           int64_t H, fmlp_stream_t s) {
+  // the shape checks come first, so a bad size reports FMLP_ERR_SHAPE, not a scratch overflow
+  const int shape = validate_block_dims(T, D, H);
+  if (shape != FMLP_OK) return static_cast<fmlp_status>(shape);
   const size_t need = fmlp_geglu_workspace_size(T, D, H);
   if (need > kNoAllocScratchBytes) {
     record_error("fmlp_geglu_noalloc: T*H*2 = %zu bytes of intermediate exceed the fixed "

@@ -21,6 +21,8 @@ enum WaitSite : int {
   SITE_DRAIN = 6,
   SITE_SMALL = 7,
   SITE_GEMV = 8,
+  SITE_DECODE_W2 = 9,
+  SITE_DECODE_BARRIER = 10,
 };
 constexpr int kDeviceTimeoutCode = 7;  // FMLP_ERR_DEVICE_TIMEOUT
 

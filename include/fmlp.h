@@ -19,12 +19,13 @@
  *                      the GELU (the same article's two-layer ReLU MLP).
  *   fmlp_moe_geglu     a mixture of experts, each a GeGLU block over the tokens routed to it
  *                      (the same article's MoE note), one launch per stage over all experts.
- *   fmlp_linear_bias_strided  fmlp_linear_bias on row-strided views (section "What's the
+ *   fmlp_*_strided     the calls above on row-strided views of x and y (section "What's the
  *                      transpose doing?").
  *
  * Common conventions
- *   - Tensors are dense, row-major (last index fastest), contiguous (except the views of
- *     fmlp_linear_bias_strided), bfloat16 bit patterns in device memory. x is [T, in]; weights use the nn.Linear layout [out, in]; biases [out].
+ *   - Tensors are dense, row-major (last index fastest), contiguous (except the x and y views
+ *     of the *_strided calls), bfloat16 bit patterns in device memory. x is [T, in]; weights
+ *     use the nn.Linear layout [out, in]; biases [out].
  *     T is the token count batch*seq (section "Why are there two kinds of GEMM kernels?").
  *   - Accumulation is fp32. The bias is added in fp32 before the activation. The output and
  *     the one intermediate (m or h) are each rounded to bf16 once, round-to-nearest-even.
@@ -32,9 +33,16 @@
  *     and launches only hand-written kernels. Results are valid once `s` has synchronised.
  *     Results are deterministic: no atomics take part in any sum.
  *   - Ownership: all tensor and workspace pointers belong to the caller; the library keeps
- *     none of them after the call returns. The library owns only per-device caches (SM count,
- *     CUDA function attributes, encoded tensor maps), guarded by a mutex; the calls are
- *     thread-safe.
+ *     none of them after the call returns. The library owns host caches (per device: SM
+ *     count, CUDA function attributes, the stream -> barrier-counter table of the decode plan;
+ *     per process: encoded TMA tensor maps, keyed by address, sizes, strides and box, so an
+ *     entry is valid for any buffer at that address with those sizes), guarded by mutexes, and three arrays of its own device memory on every GPU it runs on,
+ *     held until the process exits: the status word below, the decode plan's grid-barrier
+ *     counters (1024 x 128 bytes), and the 64 MiB scratch of fmlp_geglu_noalloc. The calls
+ *     are thread-safe, with two exceptions stated where they apply: fmlp_geglu_noalloc calls
+ *     must not overlap on the GPU, and FMLP_PLAN_DECODE keeps one barrier counter per stream.
+ *     The library looks up the device addresses of its arrays once per device; a device reset
+ *     (cudaDeviceReset) while the library is loaded leaves them stale and is not supported.
  *   - Requirements checked before anything is launched (the status names the first failure):
  *       FMLP_ERR_NULL       a required pointer is NULL
  *       FMLP_ERR_SHAPE      T < 0, or an inner dimension (in/out/D/H/Dout) < 1 or not a
@@ -94,8 +102,11 @@ typedef enum {
                                    tokens, the batched ones above); GeGLU/MLP: 2 kernels,
                                    m/h in ws */
     FMLP_PLAN_FUSED_SMALL = 2,  /* GeGLU: whole block in 1 kernel, m kept on chip */
-    FMLP_PLAN_GEMV = 3          /* one token (two when the call's weights are <= 16 MiB):
+    FMLP_PLAN_GEMV = 3,         /* one token (two when the call's weights are <= 16 MiB):
                                    weight-streaming GEMV kernel(s) */
+    FMLP_PLAN_DECODE = 4        /* GeGLU/MLP, 1..4 tokens: both layers in one weight-streaming
+                                   kernel (one CTA per SM, a grid barrier between the layers),
+                                   h/m in ws */
 } fmlp_plan;
 
 /* y[T, out] = bf16(x[T, in] @ W[out, in]^T + b[out]).
@@ -130,9 +141,21 @@ FMLP_API fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const voi
 
 /* y[T, D] = bf16(m Wd[D, H]^T) with m = bf16(gelu_tanh(x Wg^T) * (x Wu^T)); bias-free, as in
  * the page's SimpleGeGLUMLP. ws: device workspace of at least
- * fmlp_geglu_workspace_size(T, D, H) bytes, 256-byte aligned, that holds m between the two
- * kernels of the TC plan; NULL with ws_bytes == 0 lets the library take it from the stream-
- * ordered allocator (cudaMallocAsync/cudaFreeAsync on `s`). */
+ * fmlp_geglu_workspace_size(T, D, H) bytes, 256-byte aligned, that holds m between the
+ * stages (every plan but FMLP_PLAN_FUSED_SMALL); NULL with ws_bytes == 0 lets the library
+ * take it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `s`).
+ *
+ * Decode plan (1..4 tokens, FMLP_PLAN_DECODE; also fmlp_mlp_gelu): one kernel whose thread
+ * blocks, one per SM and all resident at once, meet at a grid barrier between the layers.
+ * The barrier is a counter in the library's device memory that belongs to the calling
+ * stream (the first 1024 streams that call it on a device get one each; later streams take
+ * the two-kernel plans). Calls on one stream are ordered and share the counter safely; calls
+ * on different streams use different counters. Work captured into a CUDA graph keeps the
+ * counter of the stream it was captured on, so two graphs captured on one stream must not run
+ * at the same time as each other or as calls on that stream. The barrier wait is bounded
+ * like every device wait: if other work keeps some of the kernel's thread blocks from
+ * becoming resident for about a second, the call reports FMLP_ERR_DEVICE_TIMEOUT through
+ * fmlp_device_status() and its output is undefined. */
 FMLP_API fmlp_status fmlp_geglu(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
                        int64_t T, int64_t D, int64_t H, void* ws, size_t ws_bytes,
                        fmlp_stream_t s);
@@ -144,6 +167,23 @@ FMLP_API fmlp_status fmlp_mlp_gelu(const void* x, const void* W1, const void* b1
                           const void* b2, void* y, int64_t T, int64_t D, int64_t H,
                           int64_t Dout, fmlp_gelu_mode mode, void* ws, size_t ws_bytes,
                           fmlp_stream_t s);
+
+/* fmlp_geglu and fmlp_mlp_gelu on row-strided views of x and y: row t of x starts at
+ * x + t * ldx and row t of y at y + t * ldy (in elements), as with slices of wider tensors
+ * (section "What's the transpose doing?": strides describe a view without moving data). The
+ * same rules as fmlp_linear_bias_strided: ldx >= D and ldy >= D (Dout for the MLP), else
+ * FMLP_ERR_SHAPE; multiples of 8, else FMLP_ERR_ALIGN; 0 means packed rows; y must not share
+ * an element with any input or the workspace. Weights, biases and the workspace stay packed.
+ * Same plans and kernels as the packed calls. */
+FMLP_API fmlp_status fmlp_geglu_strided(const void* x, int64_t ldx, const void* Wg,
+                                        const void* Wu, const void* Wd, void* y, int64_t ldy,
+                                        int64_t T, int64_t D, int64_t H, void* ws,
+                                        size_t ws_bytes, fmlp_stream_t s);
+FMLP_API fmlp_status fmlp_mlp_gelu_strided(const void* x, int64_t ldx, const void* W1,
+                                           const void* b1, const void* W2, const void* b2,
+                                           void* y, int64_t ldy, int64_t T, int64_t D, int64_t H,
+                                           int64_t Dout, fmlp_gelu_mode mode, void* ws,
+                                           size_t ws_bytes, fmlp_stream_t s);
 
 /* Mixture-of-experts feed-forward: E experts, each a GeGLU block (the ainews.cool article's MoE
  * note: every expert is an MLP, and fusing them cuts per-expert overhead). The tokens are
@@ -165,15 +205,16 @@ FMLP_API size_t fmlp_moe_geglu_workspace_size(int64_t T, int64_t D, int64_t H);
 /* fmlp_geglu for callers that cannot allocate device memory (no counterpart in the pages).
  *
  * Who needs it: code that may not call cudaMalloc or any allocating routine - a plugin in a
- * serving process whose memory pool owns the device, a real-time loop that must not risk an
- * allocation stall or failure, work being recorded into a CUDA graph. fmlp_geglu keeps the
- * intermediate m in a caller workspace (or allocates one); this call keeps it in a fixed
+ * serving process whose memory pool owns the device and forbids allocations after start-up,
+ * or a real-time loop that must not risk an allocation stall or failure. fmlp_geglu keeps
+ * the intermediate m in a caller workspace (or allocates one); this call keeps it in a fixed
  * 64 MiB array of device memory that belongs to the library, and allocates nothing: it
  * calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * Same arguments, layouts and results as fmlp_geglu without ws/ws_bytes. Limit:
- * fmlp_geglu_workspace_size(T, D, H) <= 64 MiB (e.g. T*H <= 32M); larger sizes return
- * FMLP_ERR_WORKSPACE without launching anything. Every GPU that loads the library holds the
+ * Same arguments, layouts and results as fmlp_geglu without ws/ws_bytes. The shape checks
+ * come first (FMLP_ERR_SHAPE as for fmlp_geglu). Limit: fmlp_geglu_workspace_size(T, D, H)
+ * <= 64 MiB (e.g. T*H <= 32M); larger sizes return FMLP_ERR_WORKSPACE without launching
+ * anything. Every GPU that loads the library holds the
  * 64 MiB array until the process exits. All calls share the array (it keeps the last call's
  * m; every call overwrites all of m it reads, so nothing needs clearing): calls whose kernels
  * can overlap on the GPU - on different streams, or from different threads without ordering -
@@ -217,6 +258,37 @@ FMLP_API fmlp_status fmlp_gelu_eval(const float* in, float* out, int64_t n, fmlp
  * FMLP_OK, or FMLP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
  * call (which wait is named in fmlp_last_error()). */
 FMLP_API fmlp_status fmlp_device_status(fmlp_stream_t s);
+
+/* Failure-injection test hooks, process-wide, all off by default. Neither faults nor hangs a
+ * GPU: the failures are made on the host, or by a bounded device wait that runs out.
+ *   FMLP_INJECT_NONE       clear every injection (count and timeout_us ignored).
+ *   FMLP_INJECT_LAUNCH     the next `count` kernel launches of the library fail on the host as
+ *                          a refused launch would: nothing is launched, the call returns
+ *                          FMLP_ERR_CUDA and fmlp_last_error() says "injected". A block call
+ *                          whose second kernel is refused has launched its first.
+ *   FMLP_INJECT_SKIP_LOAD  the next `count` launches of the CTA-pair tcgen05 GEMM (the batched
+ *                          tile kernel) expect the bytes of their first K step but issue no
+ *                          load for it, with every device wait of those launches bounded by
+ *                          timeout_us (0: about one second): the MMA's wait on that stage runs
+ *                          out, the producer's and the epilogue's waits follow, the kernel
+ *                          records FMLP_ERR_DEVICE_TIMEOUT (read by fmlp_device_status()) and
+ *                          returns with its output undefined.
+ * count in [0, 1000000], timeout_us in [0, 2000000], kind known; else FMLP_ERR_SHAPE. */
+typedef enum {
+    FMLP_INJECT_NONE = 0,
+    FMLP_INJECT_LAUNCH = 1,
+    FMLP_INJECT_SKIP_LOAD = 2
+} fmlp_inject_kind;
+FMLP_API fmlp_status fmlp_test_inject(int kind, int64_t count, int64_t timeout_us);
+
+/* Test hook for the one-kernel decode plan (FMLP_PLAN_DECODE), process-wide: later decode
+ * launches add extra_ctas CTAs beyond the ones that can be resident at once, so the resident
+ * CTAs wait at the grid barrier for CTAs that cannot start until they leave, and every device
+ * wait of those launches is bounded by timeout_us (0: the default of about one second). The
+ * waits run out, the kernel records FMLP_ERR_DEVICE_TIMEOUT and returns; the output is then
+ * undefined; nothing faults or hangs. (0, 0) restores normal launches. extra_ctas in
+ * [0, 4096], timeout_us in [0, 2000000], else FMLP_ERR_SHAPE. */
+FMLP_API fmlp_status fmlp_test_decode_overload(int64_t extra_ctas, int64_t timeout_us);
 
 /* Test hook for the bounded-wait machinery: launches one CTA whose thread waits on an
  * mbarrier that nothing completes, with a limit of timeout_us microseconds (1..2,000,000).

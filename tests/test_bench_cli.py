@@ -34,3 +34,21 @@ def test_defaults_warm_up_at_least_three_steps(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse()
     assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
+
+
+def test_peak_basis_follows_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.bf16_peak_basis(0.13) == ("bf16_tflops", "burst")
+    assert bench.bf16_peak_basis(2.5) == ("bf16_tflops_sustained", "sustained")
+
+
+def test_error_stats_of_bf16_bits():
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    ref = np.array([0x3F80, 0x4000, 0xBF80, 0x0000], dtype=np.uint16)     # 1, 2, -1, 0
+    got = np.array([0x3F81, 0x4000, 0xBF80, 0x0000], dtype=np.uint16)     # 1 + 2^-7
+    st = bench.error_stats(np, got, ref, "four values")
+    assert st["max_abs"] == 2.0 ** -7 and st["max_ulp"] == 1 and st["mismatch_bits"] == 1
+    assert abs(st["frob_rel"] - 2.0 ** -7 / 6 ** 0.5) < 1e-12

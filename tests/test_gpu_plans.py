@@ -80,24 +80,74 @@ def test_fused_small_workload_and_determinism():
     assert_parity(a, oracle.geglu(t["x"], t["Wg"], t["Wu"], t["Wd"]), "geglu 1024x32x64")
 
 
+# (T, D, H, Dout): the 1024 x 32 -> 64 -> 32 block; D a multiple of 8 only and H not a
+# multiple of the 64-wide hidden chunk; the widest block the plan takes; a few tokens with tiny
+# weights (which stay on this kernel rather than the decode one)
+MLP_SMALL = [(1024, 32, 64, 32), (100, 40, 72, 48), (129, 256, 2048, 256), (300, 128, 1000, 64),
+             (5, 64, 128, 16), (3, 32, 64, 32)]
+
+
+@pytest.mark.parametrize("T,D,H,Dout", MLP_SMALL)
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_TANH, fm.FMLP_GELU_ERF, fm.FMLP_RELU])
+def test_fused_small_mlp_vs_oracle(T, D, H, Dout, mode):
+    """Linear -> activation -> Linear with both biases in one kernel: h stays on chip."""
+    assert fm.fmlp_mlp_gelu_plan(T, D, H, Dout) == fm.FMLP_PLAN_FUSED_SMALL
+    assert fm.fmlp_mlp_gelu_workspace_size(T, D, H, Dout) == 0
+    x = rbits((T, D))
+    W1, b1 = ubits((H, D), 1 / math.sqrt(D)), ubits((H,), 1 / math.sqrt(D))
+    W2, b2 = ubits((Dout, H), 1 / math.sqrt(H)), ubits((Dout,), 1 / math.sqrt(H))
+    _, y, check = guarded_bf16(T, Dout)
+    fm.fmlp_mlp_gelu(to_dev(x), to_dev(W1), to_dev(b1), to_dev(W2), to_dev(b2), y, T, D, H, Dout,
+                     mode, None, 0)
+    torch.cuda.synchronize()
+    check()
+    om = {0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode]
+    assert_parity(to_host(y), oracle.mlp_gelu(x, W1, b1, W2, b2, gelu_mode=om),
+                  f"fused mlp {T}x{D}x{H}x{Dout} mode {mode}")
+
+
+def test_fused_small_mlp_nullable_biases_and_one_kernel():
+    T, D, H, Dout = 1024, 32, 64, 32
+    x = rbits((T, D))
+    W1, b1 = ubits((H, D), 1 / math.sqrt(D)), ubits((H,), 1 / math.sqrt(D))
+    W2, b2 = ubits((Dout, H), 1 / math.sqrt(H)), ubits((Dout,), 1 / math.sqrt(H))
+    dx, dW1, db1, dW2, db2 = (to_dev(a) for a in (x, W1, b1, W2, b2))
+    for bb1, bb2 in ((None, db2), (db1, None), (None, None)):
+        y = empty_bf16(T, Dout)
+        fm.fmlp_mlp_gelu(dx, dW1, bb1, dW2, bb2, y, T, D, H, Dout, fm.FMLP_GELU_ERF, None, 0)
+        torch.cuda.synchronize()
+        ref = oracle.mlp_gelu(x, W1, None if bb1 is None else b1, W2, None if bb2 is None else b2,
+                              gelu_mode=oracle.GELU_ERF)
+        assert_parity(to_host(y), ref, f"fused mlp biases {bb1 is not None} {bb2 is not None}")
+    y = empty_bf16(T, Dout)
+    nk, nall = count_graph_kernels(lambda s: fm.fmlp_mlp_gelu(
+        dx, dW1, db1, dW2, db2, y, T, D, H, Dout, fm.FMLP_GELU_ERF, None, 0, stream=s))
+    assert nk == 1 and nall == 1
+
+
 # ------------------------------------------------------------------------ decode sizes
 
 SMALL_WEIGHTS = 16 << 20   # the GEMV serves two tokens when a call's weights fit in this
 
 
 def decode_plan(T, weight_bytes):
-    """The plan the decode crossover picks: the GEMV at one token, and at two when the weights
-    are small; the few-token tcgen05 kernel (a TC plan) otherwise."""
+    """The plan a single Linear takes at a few tokens: the GEMV at one token, and at two when
+    the weights are small; the few-token tcgen05 kernel (a TC plan) otherwise."""
     gemv = T == 1 or (T == 2 and weight_bytes <= SMALL_WEIGHTS)
     return fm.FMLP_PLAN_GEMV if gemv else fm.FMLP_PLAN_TC
 
 
 def test_decode_crossover_table():
-    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_GEMV
-    assert fm.fmlp_mlp_gelu_plan(2, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
-    assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_GEMV
-    assert fm.fmlp_geglu_plan(3, 768, 3072) == fm.FMLP_PLAN_TC
-    assert "few-token" in fm.fmlp_describe_plan("mlp", 4, 4096, 4096, 4096)
+    """Blocks (GeGLU, MLP) of 1..4 tokens run as one decode kernel, except tiny GeGLU blocks
+    that the single-CTA fused kernel takes; 5..128 tokens run the few-token kernels."""
+    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_mlp_gelu_plan(5, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_geglu_plan(5, 768, 3072) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(1, 32, 64) == fm.FMLP_PLAN_FUSED_SMALL
+    assert "one weight-streaming kernel" in fm.fmlp_describe_plan("mlp", 4, 4096, 4096, 4096)
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 5, 4096, 4096, 4096)
     assert "few-token" in fm.fmlp_describe_plan("mlp", 128, 4096, 4096, 4096)
     assert "few-token" not in fm.fmlp_describe_plan("mlp", 129, 4096, 4096, 4096)
 
@@ -115,22 +165,24 @@ def test_gemv_linear_vs_oracle(T, K, N):
 
 
 @pytest.mark.parametrize("T,D,H", [(1, 256, 512), (2, 768, 3072), (4, 512, 1280)])
-def test_gemv_geglu_vs_oracle(T, D, H):
-    assert fm.fmlp_geglu_plan(T, D, H) == decode_plan(T, 3 * D * H * 2)
+def test_few_token_geglu_block_and_gemv_gate_up(T, D, H):
+    """The block at a few tokens (the decode kernel, or the single-CTA fused kernel for tiny
+    weights) and the gate/up stage on its own (the GEMV at one or two tokens) against the
+    oracle."""
+    assert fm.fmlp_geglu_plan(T, D, H) in (fm.FMLP_PLAN_DECODE, fm.FMLP_PLAN_FUSED_SMALL)
     x, Wg, Wu, Wd = geglu_inputs(T, D, H)
-    assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"gemv geglu {T}x{D}x{H}")
-    # the gate/up stage on its own
+    assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"geglu {T}x{D}x{H}")
     m = empty_bf16(T, H)
     fm.fmlp_geglu_gate_up(to_dev(x), to_dev(Wg), to_dev(Wu), m, T, D, H)
     torch.cuda.synchronize()
     _, ref_m = oracle.geglu(x, Wg, Wu, Wd, want_m=True)
-    assert_parity(to_host(m), ref_m, "gemv gate/up")
+    assert_parity(to_host(m), ref_m, "gate/up")
 
 
 @pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH, fm.FMLP_RELU])
 def test_decode_mlp_4096_vs_oracle(mode):
     w = synth.WORKLOADS["mlp_4096_t1"]
-    assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == fm.FMLP_PLAN_DECODE
     t = w.generate()
     d = {k: to_dev(v) for k, v in t.items()}
     _, y, check = guarded_bf16(1, w.Dout)
@@ -159,7 +211,7 @@ def test_gemv_deterministic_across_calls():
 
 @pytest.mark.parametrize("T,D,H,plan,kernels", [
     (1024, 32, 64, fm.FMLP_PLAN_FUSED_SMALL, 1),
-    (1, 768, 3072, fm.FMLP_PLAN_GEMV, 2),
+    (1, 768, 3072, fm.FMLP_PLAN_DECODE, 1),
     (512, 768, 3072, fm.FMLP_PLAN_TC, 2),
 ])
 def test_geglu_kernel_count(T, D, H, plan, kernels):
@@ -185,7 +237,7 @@ def test_linear_and_mlp_kernel_counts():
     ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, 4096, 4096, 4096))
     nk, _ = count_graph_kernels(lambda s: fm.fmlp_mlp_gelu(
         x1, W1, b1, W2, b2, y1, 1, 4096, 4096, 4096, fm.FMLP_GELU_ERF, ws, ws.numel(), stream=s))
-    assert nk == 2     # one GEMV per layer, chained by programmatic launch
+    assert nk == 1     # both layers in one decode kernel
 
 
 def test_decode_repeated_and_on_two_streams():
@@ -242,8 +294,8 @@ def test_decode_weights_written_by_previous_kernels():
     assert np.any(W2_bits != 0)
     assert_parity(to_host(y), oracle.mlp_gelu(x, W1, b1, W2_bits, b2), "decode after linear")
 
-    # (2) W2 of block B [8, 2048] is y [4, 4096] of decode block A, queued right before B
-    TA, DA, HA, DoA = 4, 1024, 2048, 4096
+    # (2) W2 of block B [8, 2048] is y [8, 2048] of few-token block A, queued right before B
+    TA, DA, HA, DoA = 8, 1024, 2048, 2048
     xa, W1a, b1a = rbits((TA, DA)), ubits((HA, DA), 1 / 32), ubits((HA,), 1 / 32)
     W2a, b2a = ubits((DoA, HA), 1 / 45), ubits((DoA,), 1 / 45)
     DB, HB, DoB = 512, 2048, 8
@@ -254,9 +306,9 @@ def test_decode_weights_written_by_previous_kernels():
     yB = empty_bf16(1, DoB)
     wsA = workspace(fm.fmlp_mlp_gelu_workspace_size(TA, DA, HA, DoA))
     wsB = workspace(fm.fmlp_mlp_gelu_workspace_size(1, DB, HB, DoB))
-    # block A runs the few-token tcgen05 kernels, block B the GEMVs
+    # block A runs the few-token tcgen05 kernels, block B the one-kernel decode
     assert fm.fmlp_mlp_gelu_plan(TA, DA, HA, DoA) == fm.FMLP_PLAN_TC
-    assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == fm.FMLP_PLAN_DECODE
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for _ in range(3):   # repeated, so that earlier blocks' kernels overlap later ones

@@ -30,6 +30,7 @@ __all__ = [
     "FMLP_ERR_WORKSPACE", "FMLP_ERR_CUDA", "FMLP_ERR_DEVICE_TIMEOUT", "FMLP_ERR_DEVICE",
     "FMLP_GELU_TANH", "FMLP_GELU_ERF", "FMLP_PLAN_NONE", "FMLP_PLAN_TC",
     "FMLP_PLAN_FUSED_SMALL", "FMLP_PLAN_GEMV", "FMLP_PLAN_DECODE", "fmlp_test_decode_overload",
+    "fmlp_test_prefer_decode",
     "fmlp_test_inject", "FMLP_INJECT_NONE", "FMLP_INJECT_LAUNCH", "FMLP_INJECT_SKIP_LOAD",
 ]
 
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "fmlp_device_status": (_INT, [_P]),
     "fmlp_test_wait_timeout": (_INT, [_I64, _P]),
     "fmlp_test_decode_overload": (_INT, [_I64, _I64]),
+    "fmlp_test_prefer_decode": (_INT, [_INT]),
     "fmlp_test_inject": (_INT, [_INT, _I64, _I64]),
     "fmlp_status_string": (ctypes.c_char_p, [_INT]),
     "fmlp_last_error": (ctypes.c_char_p, []),
@@ -315,6 +317,12 @@ def fmlp_test_decode_overload(extra_ctas, timeout_us, raise_on_error=True):
     and a wait limit of timeout_us (0: default); (0, 0) restores normal launches."""
     st = load().fmlp_test_decode_overload(int(extra_ctas), int(timeout_us))
     return _check(st, "fmlp_test_decode_overload", raise_on_error)
+
+
+def fmlp_test_prefer_decode(on, raise_on_error=True):
+    """Route 1..4-token GeGLU/MLP blocks to the one-kernel decode (process-wide switch)."""
+    st = load().fmlp_test_prefer_decode(int(on))
+    return _check(st, "fmlp_test_prefer_decode", raise_on_error)
 
 
 def fmlp_test_wait_timeout(timeout_us, stream=None, raise_on_error=True):

@@ -60,6 +60,9 @@ struct DeviceState {
 
 // Test hook of the one-kernel decode: extra CTAs beyond the resident ones, and the wait limit.
 std::atomic<int> g_decode_extra_ctas{0};
+// Whether blocks of 1..4 tokens take the one-kernel decode when it accepts the shape (off:
+// the two-launch plans, measured faster on GB300; see fmlp_test_prefer_decode).
+std::atomic<int> g_prefer_decode{0};
 std::atomic<unsigned long long> g_decode_timeout_ns{0};
 
 // Failure-injection test hooks (fmlp_test_inject): launches left to fail on the host, CTA-pair
@@ -535,8 +538,8 @@ int plan_sms() {
 bool decode_ok(int64_t T, int64_t D, int64_t H, int64_t Dout, int nmat, int sms) {
   return T >= 1 && T <= kDecodeMaxT && D >= 8 && D % 8 == 0 && H >= 8 && H % 8 == 0 &&
          D <= kMaxDim && H <= kMaxDim && Dout >= 1 && Dout <= kMaxDim &&
-         decode_smem_bytes(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
-                           static_cast<int>(Dout), nmat, sms) <= kDecodeMaxSmem;
+         decode_ring_stages(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
+                            static_cast<int>(Dout), nmat, sms) >= 2;
 }
 
 // Decode crossover, measured on GB300 (CUDA graphs of 20 calls over 5 weight sets): the GEMV
@@ -579,7 +582,8 @@ bool fused_small(int64_t T, int64_t D, int64_t H, int64_t Dout, bool mlp) {
 int plan_mlp(int64_t T, int64_t D, int64_t H, int64_t Dout, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
   if (fused_small(T, D, H, Dout, true)) return FMLP_PLAN_FUSED_SMALL;
-  if (decode_ok(T, D, H, Dout, 1, sms)) return FMLP_PLAN_DECODE;
+  if (g_prefer_decode.load(std::memory_order_relaxed) && decode_ok(T, D, H, Dout, 1, sms))
+    return FMLP_PLAN_DECODE;
   if (gemv_ok(T, D, H, 1, sms) && gemv_ok(T, H, Dout, 1, sms) &&
       gemv_preferred(T, mat_bytes(H, D) + mat_bytes(Dout, H)))
     return FMLP_PLAN_GEMV;
@@ -589,7 +593,8 @@ int plan_mlp(int64_t T, int64_t D, int64_t H, int64_t Dout, int sms) {
 int plan_geglu(int64_t T, int64_t D, int64_t H, int sms) {
   if (T <= 0) return FMLP_PLAN_NONE;
   if (fused_small(T, D, H, D, false)) return FMLP_PLAN_FUSED_SMALL;
-  if (decode_ok(T, D, H, D, 2, sms)) return FMLP_PLAN_DECODE;
+  if (g_prefer_decode.load(std::memory_order_relaxed) && decode_ok(T, D, H, D, 2, sms))
+    return FMLP_PLAN_DECODE;
   if (T <= kGemvMaxT && D % 256 == 0 && H % 256 == 0 && gemv_ok(T, D, H, 2, sms) &&
       gemv_ok(T, H, D, 1, sms) && gemv_preferred(T, 3 * mat_bytes(H, D)))
     return FMLP_PLAN_GEMV;
@@ -1175,11 +1180,11 @@ static std::string describe_decode(const DeviceState& d, const char* name, int64
   char b[256];
   snprintf(b, sizeof b,
            "%s: one weight-streaming kernel for both layers (grid barrier between them), "
-           "T=%lld D=%lld H=%lld Dout=%lld, grid=%d, shared memory per CTA=%zu bytes",
+           "T=%lld D=%lld H=%lld Dout=%lld, grid=%d, ring of %d x 32 KB bulk-copy stages",
            name, static_cast<long long>(T), static_cast<long long>(D), static_cast<long long>(H),
            static_cast<long long>(Dout), d.sms,
-           decode_smem_bytes(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
-                             static_cast<int>(Dout), nmat, d.sms));
+           decode_ring_stages(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
+                              static_cast<int>(Dout), nmat, d.sms));
   return b;
 }
 
@@ -1331,6 +1336,16 @@ fmlp_status fmlp_test_decode_overload(int64_t extra_ctas, int64_t timeout_us) {
   g_decode_extra_ctas.store(static_cast<int>(extra_ctas), std::memory_order_relaxed);
   g_decode_timeout_ns.store(static_cast<unsigned long long>(timeout_us) * 1000ull,
                             std::memory_order_relaxed);
+  return FMLP_OK;
+}
+
+fmlp_status fmlp_test_prefer_decode(int on) {
+  t_last_error.clear();
+  if (on != 0 && on != 1) {
+    set_error("on = %d, expected 0 or 1", on);
+    return FMLP_ERR_SHAPE;
+  }
+  g_prefer_decode.store(on, std::memory_order_relaxed);
   return FMLP_OK;
 }
 

@@ -44,37 +44,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ float dot8(uint4 w, uint4 x, float s) {
-  s = fmaf(bf16_lo(w.x), bf16_lo(x.x), s);
-  s = fmaf(bf16_hi(w.x), bf16_hi(x.x), s);
-  s = fmaf(bf16_lo(w.y), bf16_lo(x.y), s);
-  s = fmaf(bf16_hi(w.y), bf16_hi(x.y), s);
-  s = fmaf(bf16_lo(w.z), bf16_lo(x.z), s);
-  s = fmaf(bf16_hi(w.z), bf16_hi(x.z), s);
-  s = fmaf(bf16_lo(w.w), bf16_lo(x.w), s);
-  s = fmaf(bf16_hi(w.w), bf16_hi(x.w), s);
-  return s;
-}
-
-// Reduce a warp's per-lane sums (one per token), store them at part[pi .. pi+T), and clear
-// the accumulators.
-template <int TMAX>
-__device__ __forceinline__ void flush_piece(float (&acc)[TMAX], float* part, size_t pi, int T,
-                                            int lane) {
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-      if (t < T) part[pi + t] = acc[t];
-  }
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-}
-
 __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -83,10 +52,26 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   return v;
 }
 
+// acc (even, odd element sums) += the 8 products of weight chunk w and x chunk (xa, xb).
+__device__ __forceinline__ void dot8x2(float2& acc, uint4 w, const float4& xa, const float4& xb) {
+  ffma2(acc, bf16_lo(w.x), bf16_hi(w.x), xa.x, xa.y);
+  ffma2(acc, bf16_lo(w.y), bf16_hi(w.y), xa.z, xa.w);
+  ffma2(acc, bf16_lo(w.z), bf16_hi(w.z), xb.x, xb.y);
+  ffma2(acc, bf16_lo(w.w), bf16_hi(w.w), xb.z, xb.w);
+}
+
 // One layer for this CTA's rows [r0, r1) of W (NMAT matrices): y[t, n] for n in [r0, r1).
 // All threads of the CTA take part (it synchronises internally). x, which the kernel this one
 // waited for may have written, is read through L2 (never a possibly stale L1 line).
-template <int EPI, int NMAT, int TMAX>
+//
+// x sits in shared memory widened to fp32 (XF32) or as bf16 (when fp32 would not leave room
+// for two CTAs per SM). The fp32 copy is split by halves of each 16-byte chunk: token t's
+// chunk c is lo = elements 8c..8c+3 at float4 index t * 2C + c and hi = 8c+4..8c+7 at
+// t * 2C + C + c (C = K / 8), so a warp's lanes, on consecutive chunks, read consecutive
+// 16-byte words. The streaming loop walks (matrix, row, segment) with a cursor advanced by
+// additions only: a division by the run-time segment count per segment used to cost more
+// instructions than the multiply-adds.
+template <int EPI, int NMAT, int TMAX, bool XF32>
 __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __restrict__ x,
                                           const __nv_bfloat16* __restrict__ W0,
                                           const __nv_bfloat16* __restrict__ W1,
@@ -97,8 +82,10 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   const int segs = K / kSeg;
   const int per_mat = rows * segs;
   const int total = NMAT * per_mat;          // segments this CTA streams
-  uint4* xs = reinterpret_cast<uint4*>(gsm);                                     // [T][K/8]
-  float* part = reinterpret_cast<float*>(gsm + static_cast<size_t>(T) * K * 2);  // [seg][T]
+  const int C = K / 8;
+  const size_t xbytes = static_cast<size_t>(T) * K * (XF32 ? 4 : 2);
+  float* part = reinterpret_cast<float*>(gsm + xbytes);  // [seg][T]
+  const uint32_t xs = smem_u32(gsm);
 
   // warp w streams segments [g0, g1) of the CTA's list (matrix-major, then row, then segment)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,32 +110,65 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   };
   load_batch(g0);   // in flight while x is staged
 
-  // x rows are ldx elements apart (a multiple of 8); xs packs them
-  const int kvec = K / 8, xvec = T * kvec;
-  for (int i = threadIdx.x; i < xvec; i += kGemvThreads) {
-    const int t = i / kvec;
-    xs[i] = ld_cg_v4(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * ldx) + (i - t * kvec));
+  // x rows are ldx elements apart (a multiple of 8)
+  for (int i = threadIdx.x; i < T * C; i += kGemvThreads) {
+    const int t = i / C, c = i - t * C;
+    const uint4 v = ld_cg_v4(x + static_cast<size_t>(t) * ldx + static_cast<size_t>(c) * 8);
+    if (XF32) {
+      float4* xf = reinterpret_cast<float4*>(gsm);
+      xf[t * 2 * C + c] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      xf[t * 2 * C + C + c] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    } else {
+      reinterpret_cast<uint4*>(gsm)[i] = v;
+    }
   }
   __syncthreads();
 
-  float acc[TMAX];
+  // cursor of the segment being summed: matrix, row, segment within the row
+  int cmat = NMAT == 2 ? (g0 >= per_mat ? 1 : 0) : 0;
+  int crow = 0, cseg = 0;
+  if (g1 > g0) {
+    const int gm = g0 - cmat * per_mat;
+    crow = gm / segs;
+    cseg = gm - crow * segs;
+  }
+  // accumulator pairs per token (two at one token, alternating between segments, so the
+  // multiply-add chains are shorter; one at more tokens, where the tokens already interleave)
+  constexpr int NA = TMAX == 1 ? 2 : 1;
+  float2 acc[TMAX][NA];
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+    for (int k = 0; k < NA; ++k) acc[t][k] = make_float2(0.f, 0.f);
   int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
-  size_t piece_pi = 0;  // its partial index
+  int piece_pi = 0;     // its partial index
+  auto flush = [&]() {
+    float v[TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      v[t] = acc[t][0].x + acc[t][0].y;
+      if (NA == 2) v[t] += acc[t][NA - 1].x + acc[t][NA - 1].y;
+#pragma unroll
+      for (int k = 0; k < NA; ++k) acc[t][k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v[t] += __shfl_xor_sync(0xffffffffu, v[t], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t)
+        if (t < T) part[piece_pi + t] = v[t];
+    }
+  };
   for (int base = g0; base < g1; base += kGemvBatch) {
     if (base != g0) load_batch(base);
 #pragma unroll
     for (int u = 0; u < kGemvBatch; ++u) {
       const int g = base + u;
       if (g >= g1) break;  // warp-uniform
-      const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
-      const int gm = g - mat * per_mat;
-      const int row = gm / segs, seg = gm - row * segs;
-      const int rid = mat * rows + row;
-      const size_t pi = static_cast<size_t>(g) * T;
+      const int rid = cmat * rows + crow;
+      const int pi = g * T;
       if (rid != piece_row) {
-        if (piece_row >= 0) flush_piece<TMAX>(acc, part, piece_pi, T, lane);
+        if (piece_row >= 0) flush();
         piece_row = rid;
         piece_pi = pi;
       } else if (lane == 0) {
@@ -156,31 +176,61 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
         for (int t = 0; t < TMAX; ++t)
           if (t < T) part[pi + t] = 0.f;
       }
+      const uint32_t chunk = static_cast<uint32_t>(cseg * (kSeg / 8) + lane);
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t)
-        if (t < T) acc[t] = dot8(wv[u], xs[t * (K / 8) + seg * (kSeg / 8) + lane], acc[t]);
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          float4 xa, xb;
+          if (XF32) {
+            const uint32_t xt = xs + static_cast<uint32_t>(t) * static_cast<uint32_t>(C) * 32u;
+            xa = lds_f4(xt + chunk * 16u);
+            xb = lds_f4(xt + static_cast<uint32_t>(C) * 16u + chunk * 16u);
+          } else {
+            const uint4 xv = lds_v4(xs + (static_cast<uint32_t>(t) * static_cast<uint32_t>(C) +
+                                          chunk) * 16u);
+            xa = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
+            xb = make_float4(bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w));
+          }
+          dot8x2(acc[t][u % NA], wv[u], xa, xb);
+        }
+      }
+      // advance the cursor
+      if (++cseg == segs) {
+        cseg = 0;
+        if (++crow == rows) {
+          crow = 0;
+          ++cmat;
+        }
+      }
     }
   }
-  if (piece_row >= 0) flush_piece<TMAX>(acc, part, piece_pi, T, lane);
+  if (piece_row >= 0) flush();
   __syncthreads();
 
-  // one thread per (row, token): add the segments in order, then the epilogue
-  for (int i = threadIdx.x; i < rows * T; i += kGemvThreads) {
+  // one warp per (row, token): the lanes add the row's segment partials (lane l takes segments
+  // l, l + 32, ...; a fixed order: deterministic), then the epilogue
+  for (int i = warp; i < rows * T; i += kGemvWarps) {
     const int row = i / T, t = i - row * T;
     float s0 = 0.f, s1 = 0.f;
-    for (int sg = 0; sg < segs; ++sg) s0 += part[static_cast<size_t>(row * segs + sg) * T + t];
+    for (int sg = lane; sg < segs; sg += 32) s0 += part[(row * segs + sg) * T + t];
     if (NMAT == 2)
-      for (int sg = 0; sg < segs; ++sg)
-        s1 += part[static_cast<size_t>(per_mat + row * segs + sg) * T + t];
-    const int n = r0 + row;
-    float v;
-    if (EPI == EPI_GEGLU) {
-      v = gelu_tanh_f(s0) * s1;
-    } else {
-      const float z = s0 + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
-      v = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
+      for (int sg = lane; sg < segs; sg += 32) s1 += part[(per_mat + row * segs + sg) * T + t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      if (NMAT == 2) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
     }
-    y[static_cast<size_t>(t) * ldy + n] = __float2bfloat16_rn(v);
+    if (lane == 0) {
+      const int n = r0 + row;
+      float v;
+      if (EPI == EPI_GEGLU) {
+        v = gelu_tanh_f(s0) * s1;
+      } else {
+        const float z = s0 + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
+        v = EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
+      }
+      y[static_cast<size_t>(t) * ldy + n] = __float2bfloat16_rn(v);
+    }
   }
   __syncthreads();   // the shared memory may be reused by the caller
 }
@@ -189,7 +239,7 @@ __device__ __forceinline__ int split_row(int i, int N) {
   return static_cast<int>((static_cast<int64_t>(i) * N) / gridDim.x);
 }
 
-template <int EPI, int NMAT, int TMAX>
+template <int EPI, int NMAT, int TMAX, bool XF32>
 __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     gemv_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ W0,
                 const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ bias,
@@ -199,13 +249,26 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
   const int r0 = split_row(blockIdx.x, N), r1 = split_row(blockIdx.x + 1, N);
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait_primary();
-  gemv_rows<EPI, NMAT, TMAX>(gsm, x, W0, W1, bias, y, T, K, N, ldx, ldy, gelu_mode, r0, r1);
+  gemv_rows<EPI, NMAT, TMAX, XF32>(gsm, x, W0, W1, bias, y, T, K, N, ldx, ldy, gelu_mode, r0,
+                                   r1);
+}
+
+// Row partials of the CTA (its rows x segments x tokens, fp32).
+static size_t gemv_part_bytes(int T, int K, int N, int nmat, int grid) {
+  const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
+  return static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+}
+
+// x is kept as fp32 while the CTA's shared memory stays within this (two CTAs per SM fit).
+constexpr size_t kGemvTwoCtaSmem = 100 * 1024;
+
+static bool gemv_x_f32(int T, int K, int N, int nmat, int grid) {
+  return static_cast<size_t>(T) * K * 4 + gemv_part_bytes(T, K, N, nmat, grid) <= kGemvTwoCtaSmem;
 }
 
 size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid) {
-  const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
-  return static_cast<size_t>(T) * K * 2 +
-         static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+  const size_t xb = static_cast<size_t>(T) * K * (gemv_x_f32(T, K, N, nmat, grid) ? 4 : 2);
+  return xb + gemv_part_bytes(T, K, N, nmat, grid);
 }
 
 // Two CTAs per SM (each at most half of an SM's registers and threads).
@@ -217,9 +280,9 @@ int gemv_grid(int T, int K, int N, int nmat, int sms) {
   return g < N ? g : N;
 }
 
-template <int EPI, int NMAT, int TMAX>
+template <int EPI, int NMAT, int TMAX, bool XF32>
 static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
-  auto kern = gemv_kernel<EPI, NMAT, TMAX>;
+  auto kern = gemv_kernel<EPI, NMAT, TMAX, XF32>;
   static SmemAttrCache cache;
   cudaError_t e =
       set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem), cache);
@@ -242,25 +305,31 @@ static cudaError_t gemv_launch_t(const GemvLaunch& L, size_t smem) {
                             L.gelu_mode);
 }
 
-cudaError_t gemv_launch(const GemvLaunch& L) {
-  const int nmat = L.epi == EPI_GEGLU ? 2 : 1;
-  const size_t smem = gemv_smem_bytes(L.T, L.K, L.N, nmat, L.grid);
-  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || L.grid < 1 || smem > kGemvMaxSmem)
-    return cudaErrorInvalidValue;
+template <bool XF32>
+static cudaError_t gemv_dispatch(const GemvLaunch& L, size_t smem) {
   if (L.T == 1) {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1>(L, smem);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1>(L, smem);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1>(L, smem);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, 1, XF32>(L, smem);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, 1, XF32>(L, smem);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, 1, XF32>(L, smem);
     }
   } else {
     switch (L.epi) {
-      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT>(L, smem);
-      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT>(L, smem);
-      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT>(L, smem);
+      case EPI_BIAS: return gemv_launch_t<EPI_BIAS, 1, kGemvMaxT, XF32>(L, smem);
+      case EPI_BIAS_GELU: return gemv_launch_t<EPI_BIAS_GELU, 1, kGemvMaxT, XF32>(L, smem);
+      case EPI_GEGLU: return gemv_launch_t<EPI_GEGLU, 2, kGemvMaxT, XF32>(L, smem);
     }
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t gemv_launch(const GemvLaunch& L) {
+  const int nmat = L.epi == EPI_GEGLU ? 2 : 1;
+  if (L.T < 1 || L.T > kGemvMaxT || L.K % kSeg != 0 || L.grid < 1) return cudaErrorInvalidValue;
+  const size_t smem = gemv_smem_bytes(L.T, L.K, L.N, nmat, L.grid);
+  if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
+  return gemv_x_f32(L.T, L.K, L.N, nmat, L.grid) ? gemv_dispatch<true>(L, smem)
+                                                 : gemv_dispatch<false>(L, smem);
 }
 
 }  // namespace fmlp

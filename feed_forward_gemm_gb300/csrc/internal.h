@@ -121,10 +121,11 @@ size_t gemv_smem_bytes(int T, int K, int N, int nmat, int grid);
 cudaError_t gemv_launch(const GemvLaunch& L);
 
 // The whole block (both layers) in one weight-streaming kernel for 1..kDecodeMaxT tokens
-// (decode.cu): one CTA per SM, every CTA resident, a bounded grid barrier between the layers.
+// (decode.cu): one CTA per SM, every CTA resident, weights streamed by bulk copies through a
+// shared-memory ring, a bounded grid barrier between the layers.
 constexpr int kDecodeMaxT = 4;
 constexpr int kDecodeSlots = 1024;           // grid-barrier counters per device
-constexpr size_t kDecodeMaxSmem = 232448;    // 227 KB: the opt-in shared memory of one CTA
+constexpr size_t kDecodeMaxSmem = 227 * 1024;   // the opt-in shared memory of one CTA
 struct DecodeLaunch {
   const void* x;      // [T, D], row stride ldx
   const void* W1a;    // [H, D]  W1 (MLP) or Wg (GeGLU)
@@ -144,13 +145,15 @@ struct DecodeLaunch {
   uint64_t timeout_ns;
   cudaStream_t stream;
 };
-// Dynamic shared memory the decode kernel needs for these sizes on `grid` CTAs (the token
-// vectors and the per-warp row sums); the plan requires it to fit in kDecodeMaxSmem.
+// Dynamic shared memory the decode kernel needs besides its ring (the token vectors and the
+// per-warp row sums), and the ring stages (whole rows, about 8 KB each) that fit beside it
+// within kDecodeMaxSmem (0: fewer than two; the plan then does not take the kernel).
 size_t decode_smem_bytes(int T, int D, int H, int Dout, int nmat, int grid);
+int decode_ring_stages(int T, int D, int H, int Dout, int nmat, int grid);
 cudaError_t decode_launch(const DecodeLaunch& L);
 // Device address of the first grid-barrier counter (slot i is at + 16 * i).
 cudaError_t decode_barrier_base(unsigned long long** p);
-// Resident CTAs per SM of the decode kernel at its largest shared memory (0: it cannot run).
+// Resident CTAs per SM of the decode kernel (0: it cannot run on this device).
 cudaError_t decode_occupancy(int* per_sm);
 
 // Whole block in one kernel for small D and Dout (fused plan): the GeGLU block, or

@@ -106,7 +106,7 @@ typedef enum {
                                    weight-streaming GEMV kernel(s) */
     FMLP_PLAN_DECODE = 4        /* GeGLU/MLP, 1..4 tokens: both layers in one weight-streaming
                                    kernel (one CTA per SM, a grid barrier between the layers),
-                                   h/m in ws */
+                                   h/m in ws; taken only after fmlp_test_prefer_decode(1) */
 } fmlp_plan;
 
 /* y[T, out] = bf16(x[T, in] @ W[out, in]^T + b[out]).
@@ -145,8 +145,10 @@ FMLP_API fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const voi
  * stages (every plan but FMLP_PLAN_FUSED_SMALL); NULL with ws_bytes == 0 lets the library
  * take it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `s`).
  *
- * Decode plan (1..4 tokens, FMLP_PLAN_DECODE; also fmlp_mlp_gelu): one kernel whose thread
- * blocks, one per SM and all resident at once, meet at a grid barrier between the layers.
+ * Decode plan (1..4 tokens, FMLP_PLAN_DECODE; also fmlp_mlp_gelu; only while
+ * fmlp_test_prefer_decode(1) is in effect, since the two-launch plans measure faster on
+ * GB300): one kernel whose thread blocks, one per SM and all resident at once, meet at a
+ * grid barrier between the layers.
  * The barrier is a counter in the library's device memory that belongs to the calling
  * stream (the first 1024 streams that call it on a device get one each; later streams take
  * the two-kernel plans). Calls on one stream are ordered and share the counter safely; calls
@@ -289,6 +291,14 @@ FMLP_API fmlp_status fmlp_test_inject(int kind, int64_t count, int64_t timeout_u
  * undefined; nothing faults or hangs. (0, 0) restores normal launches. extra_ctas in
  * [0, 4096], timeout_us in [0, 2000000], else FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_decode_overload(int64_t extra_ctas, int64_t timeout_us);
+
+/* Plan switch for the one-kernel decode, process-wide: with on = 1, GeGLU and MLP blocks of
+ * 1..4 tokens whose shapes the decode kernel accepts run as FMLP_PLAN_DECODE (plan queries
+ * report it; the workspace size is the same T * H * 2 bytes); with on = 0 (the default) they
+ * take the GEMV or the few-token tcgen05 kernels, which measure faster on GB300 (the 4096-wide
+ * MLP at one token: 19.1 us against 25.4 us). Switch it only while no other thread queries
+ * plans or launches. on not 0 or 1: FMLP_ERR_SHAPE. */
+FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
 
 /* Test hook for the bounded-wait machinery: launches one CTA whose thread waits on an
  * mbarrier that nothing completes, with a limit of timeout_us microseconds (1..2,000,000).

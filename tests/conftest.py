@@ -24,3 +24,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def prefer_decode():
+    """Blocks of 1..4 tokens take the one-kernel decode plan while the test runs."""
+    import feed_forward_gemm_gb300 as fm
+    fm.load()
+    fm.fmlp_test_prefer_decode(1)
+    yield
+    fm.fmlp_test_prefer_decode(0)

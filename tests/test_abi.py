@@ -209,17 +209,28 @@ def test_moe_validation(lib):
 
 
 def test_decode_crossover_is_pure_host(lib):
-    """Blocks of 1..4 tokens run as one decode kernel (tiny GeGLU blocks as the fused one); a
-    single Linear takes the GEMV at one token, and at two when its weights are small (<= 16
-    MiB); the tcgen05 kernels (the few-token one below 129 tokens) serve the rest."""
-    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
-    assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
+    """Blocks of 1..4 tokens take the GEMV pair at one token (and at two for small weights),
+    the few-token kernels otherwise (tiny GeGLU blocks the fused one); with the decode switch
+    on, the one-kernel decode where it accepts the shape. A single Linear takes the GEMV at
+    one token, and at two when its weights are small (<= 16 MiB); the tcgen05 kernels (the
+    few-token one below 129 tokens) serve the rest."""
+    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(1, 768, 3072) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_geglu_plan(4, 768, 3072) == fm.FMLP_PLAN_TC
+    fm.fmlp_test_prefer_decode(1)
+    try:
+        assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
+        assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
+        assert fm.fmlp_geglu_plan(1, 768, 3072) == fm.FMLP_PLAN_DECODE
+        assert fm.fmlp_geglu_plan(4, 768, 3072) == fm.FMLP_PLAN_DECODE
+        assert fm.fmlp_geglu_plan(1, 8192, 28672) == fm.FMLP_PLAN_GEMV   # no room for two stages
+    finally:
+        fm.fmlp_test_prefer_decode(0)
+    assert fm.fmlp_test_prefer_decode(2, raise_on_error=False) == fm.FMLP_ERR_SHAPE
     assert fm.fmlp_mlp_gelu_plan(5, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
-    assert fm.fmlp_geglu_plan(1, 768, 3072) == fm.FMLP_PLAN_DECODE
-    assert fm.fmlp_geglu_plan(4, 768, 3072) == fm.FMLP_PLAN_DECODE
     assert fm.fmlp_geglu_plan(5, 768, 3072) == fm.FMLP_PLAN_TC
     assert fm.fmlp_geglu_plan(1, 32, 64) == fm.FMLP_PLAN_FUSED_SMALL
-    assert fm.fmlp_geglu_plan(1, 8192, 28672) == fm.FMLP_PLAN_DECODE
     assert fm.fmlp_linear_plan(2, 4096, 4096) == fm.FMLP_PLAN_TC       # 33.6 MB
     assert fm.fmlp_linear_plan(2, 256, 64) == fm.FMLP_PLAN_GEMV
     assert fm.fmlp_linear_plan(1, 4104, 520) == fm.FMLP_PLAN_TC        # K not a multiple of 256
@@ -239,9 +250,9 @@ def test_fused_small_plans_are_shape_only(lib):
     assert fm.fmlp_mlp_gelu_plan(100, 264, 72, 48) == fm.FMLP_PLAN_TC        # D > 256
     assert fm.fmlp_mlp_gelu_plan(100, 256, 2056, 256) == fm.FMLP_PLAN_TC     # H > 2048
     assert fm.fmlp_mlp_gelu_plan(3, 32, 64, 32) == fm.FMLP_PLAN_FUSED_SMALL  # tiny weights
-    assert fm.fmlp_mlp_gelu_plan(3, 256, 2048, 256) == fm.FMLP_PLAN_DECODE   # 2 MiB of weights
+    assert fm.fmlp_mlp_gelu_plan(3, 256, 2048, 256) == fm.FMLP_PLAN_TC       # 2 MiB of weights
     assert fm.fmlp_mlp_gelu_workspace_size(3, 256, 2048, 256) == 3 * 2048 * 2
-    assert fm.fmlp_geglu_plan(3, 256, 2048) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_geglu_plan(3, 256, 2048) == fm.FMLP_PLAN_TC
     assert fm.fmlp_geglu_plan(5, 256, 2048) == fm.FMLP_PLAN_FUSED_SMALL
     assert fm.fmlp_geglu_workspace_size(5, 256, 2048) == 0
 

@@ -1,5 +1,5 @@
-"""The one-kernel decode plan (both layers of the block in one launch for 1..4 tokens) against
-the oracle: every activation, the GeGLU block, ragged and narrow shapes (rows split unevenly
+"""The one-kernel decode plan (both layers of the block in one launch for 1..4 tokens; taken
+while fmlp_test_prefer_decode(1) is in effect, as in every test here) against the oracle: every activation, the GeGLU block, ragged and narrow shapes (rows split unevenly
 over the CTAs, rows shorter than a warp's 32 chunks), rows longer than one 16-byte chunk per
 thread, nullable biases, determinism, two streams, one kernel per call, and the bounded
 grid-barrier wait running out and reporting."""
@@ -38,7 +38,9 @@ def fast_ubits(shape, bound, seed):
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     fm.load()
+    fm.fmlp_test_prefer_decode(1)
     yield
+    fm.fmlp_test_prefer_decode(0)
     fm.fmlp_test_decode_overload(0, 0)
     assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
 
@@ -109,16 +111,23 @@ def test_decode_mlp_without_biases():
 
 
 def test_decode_long_rows():
-    """H = 28672: every thread of a CTA covers several 16-byte chunks of a layer-2 row (and the
-    layer-1 rows are short enough for four thread groups per CTA)."""
-    T, D, H, Dout = 1, 1024, 28672, 8192
+    """H = 16384: a layer-2 row of 32 KB fills a ring stage by itself and every consumer thread
+    covers four 16-byte chunks of it (the layer-1 rows are short enough for four thread
+    groups)."""
+    T, D, H, Dout = 1, 1024, 16384, 4096
     assert fm.fmlp_mlp_gelu_plan(T, D, H, Dout) == fm.FMLP_PLAN_DECODE
     x = rbits((T, D))
-    W1, W2 = fast_ubits((H, D), 1 / 32, 41), fast_ubits((Dout, H), 1 / 170, 42)
+    W1, W2 = fast_ubits((H, D), 1 / 32, 41), fast_ubits((Dout, H), 1 / 128, 42)
     b1, b2 = ubits((H,), 0.05), ubits((Dout,), 0.05)
     got = run_mlp(x, W1, b1, W2, b2, fm.FMLP_GELU_ERF)
     assert_parity(got, oracle.mlp_gelu(x, W1, b1, W2, b2, gelu_mode=fm.FMLP_GELU_ERF),
                   "decode long rows")
+
+
+def test_rows_too_long_for_two_stages_take_the_gemv():
+    """With H = 40960 the token vector (80 KB) and two ring stages of one 80 KB layer-2 row do
+    not fit in shared memory: the block runs as two GEMVs."""
+    assert fm.fmlp_mlp_gelu_plan(1, 1024, 40960, 1024) == fm.FMLP_PLAN_GEMV
 
 
 @pytest.mark.parametrize("T,D,H", [(1, 768, 3072), (2, 768, 3072), (3, 768, 3072),
@@ -131,12 +140,11 @@ def test_decode_geglu_vs_oracle(T, D, H):
     assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"decode geglu {T}x{D}x{H}")
 
 
-def test_decode_geglu_70b_class_one_token():
-    """The 70B-class block (D 8192, H 28672) at one token: 1.41 GB of weights, one kernel."""
+def test_geglu_70b_class_one_token():
+    """The 70B-class block (D 8192, H 28672) at one token: 1.41 GB of weights (two GEMVs)."""
     w = synth.WORKLOADS["geglu_8192x8192x28672"]
     t = w.generate(names=["Wg", "Wu", "Wd"])
     x = rbits((1, w.D))
-    assert fm.fmlp_geglu_plan(1, w.D, w.H) == fm.FMLP_PLAN_DECODE
     assert_parity(run_geglu(x, t["Wg"], t["Wu"], t["Wd"]), oracle.geglu(x, t["Wg"], t["Wu"], t["Wd"]),
                   "decode geglu 70B-class")
 

@@ -138,18 +138,28 @@ def decode_plan(T, weight_bytes):
 
 
 def test_decode_crossover_table():
-    """Blocks (GeGLU, MLP) of 1..4 tokens run as one decode kernel, except tiny GeGLU blocks
-    that the single-CTA fused kernel takes; 5..128 tokens run the few-token kernels."""
+    """Blocks (GeGLU, MLP) of 1..4 tokens take the GEMV pair at one token (and at two for small
+    weights) and the few-token kernels otherwise, tiny GeGLU blocks the single-CTA fused
+    kernel; 5..128 tokens run the few-token kernels."""
+    assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_mlp_gelu_plan(5, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_GEMV
+    assert fm.fmlp_geglu_plan(5, 768, 3072) == fm.FMLP_PLAN_TC
+    assert fm.fmlp_geglu_plan(1, 32, 64) == fm.FMLP_PLAN_FUSED_SMALL
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 4, 4096, 4096, 4096)
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 5, 4096, 4096, 4096)
+    assert "few-token" in fm.fmlp_describe_plan("mlp", 128, 4096, 4096, 4096)
+    assert "few-token" not in fm.fmlp_describe_plan("mlp", 129, 4096, 4096, 4096)
+
+
+def test_decode_crossover_table_with_the_decode_plan(prefer_decode):
     assert fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
     assert fm.fmlp_mlp_gelu_plan(4, 4096, 4096, 4096) == fm.FMLP_PLAN_DECODE
     assert fm.fmlp_mlp_gelu_plan(5, 4096, 4096, 4096) == fm.FMLP_PLAN_TC
     assert fm.fmlp_geglu_plan(2, 768, 3072) == fm.FMLP_PLAN_DECODE
-    assert fm.fmlp_geglu_plan(5, 768, 3072) == fm.FMLP_PLAN_TC
     assert fm.fmlp_geglu_plan(1, 32, 64) == fm.FMLP_PLAN_FUSED_SMALL
     assert "one weight-streaming kernel" in fm.fmlp_describe_plan("mlp", 4, 4096, 4096, 4096)
-    assert "few-token" in fm.fmlp_describe_plan("mlp", 5, 4096, 4096, 4096)
-    assert "few-token" in fm.fmlp_describe_plan("mlp", 128, 4096, 4096, 4096)
-    assert "few-token" not in fm.fmlp_describe_plan("mlp", 129, 4096, 4096, 4096)
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4])
@@ -164,14 +174,21 @@ def test_gemv_linear_vs_oracle(T, K, N):
     assert_parity(to_host(y), oracle.linear(x, W, b), f"gemv {T}x{K}->{N}")
 
 
+@pytest.mark.parametrize("decode", [False, True])
 @pytest.mark.parametrize("T,D,H", [(1, 256, 512), (2, 768, 3072), (4, 512, 1280)])
-def test_few_token_geglu_block_and_gemv_gate_up(T, D, H):
-    """The block at a few tokens (the decode kernel, or the single-CTA fused kernel for tiny
-    weights) and the gate/up stage on its own (the GEMV at one or two tokens) against the
-    oracle."""
-    assert fm.fmlp_geglu_plan(T, D, H) in (fm.FMLP_PLAN_DECODE, fm.FMLP_PLAN_FUSED_SMALL)
-    x, Wg, Wu, Wd = geglu_inputs(T, D, H)
-    assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"geglu {T}x{D}x{H}")
+def test_few_token_geglu_block_and_gemv_gate_up(T, D, H, decode):
+    """The block at a few tokens (the default plans, or the decode kernel; the single-CTA fused
+    kernel for tiny weights either way) and the gate/up stage on its own (the GEMV at one or
+    two tokens) against the oracle."""
+    fm.fmlp_test_prefer_decode(1 if decode else 0)
+    try:
+        plans = (fm.FMLP_PLAN_DECODE, fm.FMLP_PLAN_FUSED_SMALL) if decode else \
+            (fm.FMLP_PLAN_GEMV, fm.FMLP_PLAN_TC, fm.FMLP_PLAN_FUSED_SMALL)
+        assert fm.fmlp_geglu_plan(T, D, H) in plans
+        x, Wg, Wu, Wd = geglu_inputs(T, D, H)
+        assert_parity(run_geglu(x, Wg, Wu, Wd), oracle.geglu(x, Wg, Wu, Wd), f"geglu {T}x{D}x{H}")
+    finally:
+        fm.fmlp_test_prefer_decode(0)
     m = empty_bf16(T, H)
     fm.fmlp_geglu_gate_up(to_dev(x), to_dev(Wg), to_dev(Wu), m, T, D, H)
     torch.cuda.synchronize()
@@ -179,10 +196,15 @@ def test_few_token_geglu_block_and_gemv_gate_up(T, D, H):
     assert_parity(to_host(m), ref_m, "gate/up")
 
 
+@pytest.mark.parametrize("decode", [False, True])
 @pytest.mark.parametrize("mode", [fm.FMLP_GELU_ERF, fm.FMLP_GELU_TANH, fm.FMLP_RELU])
-def test_decode_mlp_4096_vs_oracle(mode):
+def test_decode_mlp_4096_vs_oracle(mode, decode, request):
+    """The 4096-wide MLP at one token: the GEMV pair (default) and the one-kernel decode."""
+    if decode:
+        request.getfixturevalue("prefer_decode")
     w = synth.WORKLOADS["mlp_4096_t1"]
-    assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_mlp_gelu_plan(1, w.D, w.H, w.Dout) == \
+        (fm.FMLP_PLAN_DECODE if decode else fm.FMLP_PLAN_GEMV)
     t = w.generate()
     d = {k: to_dev(v) for k, v in t.items()}
     _, y, check = guarded_bf16(1, w.Dout)
@@ -212,9 +234,12 @@ def test_gemv_deterministic_across_calls():
 @pytest.mark.parametrize("T,D,H,plan,kernels", [
     (1024, 32, 64, fm.FMLP_PLAN_FUSED_SMALL, 1),
     (1, 768, 3072, fm.FMLP_PLAN_DECODE, 1),
+    (1, 768, 3072, fm.FMLP_PLAN_GEMV, 2),
     (512, 768, 3072, fm.FMLP_PLAN_TC, 2),
 ])
-def test_geglu_kernel_count(T, D, H, plan, kernels):
+def test_geglu_kernel_count(T, D, H, plan, kernels, request):
+    if plan == fm.FMLP_PLAN_DECODE:
+        request.getfixturevalue("prefer_decode")
     assert fm.fmlp_geglu_plan(T, D, H) == plan
     x, Wg, Wu, Wd = (to_dev(a) for a in geglu_inputs(T, D, H))
     y = empty_bf16(T, D)
@@ -237,12 +262,23 @@ def test_linear_and_mlp_kernel_counts():
     ws = workspace(fm.fmlp_mlp_gelu_workspace_size(1, 4096, 4096, 4096))
     nk, _ = count_graph_kernels(lambda s: fm.fmlp_mlp_gelu(
         x1, W1, b1, W2, b2, y1, 1, 4096, 4096, 4096, fm.FMLP_GELU_ERF, ws, ws.numel(), stream=s))
+    assert nk == 2     # one GEMV per layer
+    fm.fmlp_test_prefer_decode(1)
+    try:
+        nk, _ = count_graph_kernels(lambda s: fm.fmlp_mlp_gelu(
+            x1, W1, b1, W2, b2, y1, 1, 4096, 4096, 4096, fm.FMLP_GELU_ERF, ws, ws.numel(),
+            stream=s))
+    finally:
+        fm.fmlp_test_prefer_decode(0)
     assert nk == 1     # both layers in one decode kernel
 
 
-def test_decode_repeated_and_on_two_streams():
-    """Decode calls in a row, alternating between two streams: every call gives the oracle's
-    (and the first call's) result."""
+@pytest.mark.parametrize("decode", [False, True])
+def test_decode_repeated_and_on_two_streams(decode, request):
+    """Decode calls in a row (the GEMV pair, or the one-kernel decode), alternating between two
+    streams: every call gives the oracle's (and the first call's) result."""
+    if decode:
+        request.getfixturevalue("prefer_decode")
     T, D, H = 2, 1024, 2048
     x, W1, b1 = rbits((T, D)), ubits((H, D), 1 / 32), ubits((H,), 1 / 32)
     W2, b2 = ubits((D, H), 1 / 45), ubits((D,), 1 / 45)
@@ -267,12 +303,16 @@ def test_decode_repeated_and_on_two_streams():
 
 # ------------------------------------------------------------------------ decode ordering
 
-def test_decode_weights_written_by_previous_kernels():
-    """Kernels of a decode block start before the kernel queued ahead of them has finished
-    (programmatic dependent launch); they must still see weights that kernels queued just
-    before the block wrote. W2 of a block is written, on the same stream with no
-    synchronisation, first by a tensor-core Linear and then by the second GEMV of another
-    decode block; both results must match the oracle run on the weights as written."""
+@pytest.mark.parametrize("decode", [False, True])
+def test_decode_weights_written_by_previous_kernels(decode, request):
+    """Kernels of a decode block (the GEMV pair, or the one-kernel decode) start before the
+    kernel queued ahead of them has finished (programmatic dependent launch); they must still
+    see weights that kernels queued just before the block wrote. W2 of a block is written, on
+    the same stream with no synchronisation, first by a tensor-core Linear and then by the
+    last kernel of another block; both results must match the oracle run on the weights as
+    written."""
+    if decode:
+        request.getfixturevalue("prefer_decode")
     s = torch.cuda.Stream()
     # (1) W2 [1024, 2048] is the output of a tensor-core Linear queued right before the block
     Tl, Kl, Nl = 1024, 256, 2048
@@ -306,9 +346,10 @@ def test_decode_weights_written_by_previous_kernels():
     yB = empty_bf16(1, DoB)
     wsA = workspace(fm.fmlp_mlp_gelu_workspace_size(TA, DA, HA, DoA))
     wsB = workspace(fm.fmlp_mlp_gelu_workspace_size(1, DB, HB, DoB))
-    # block A runs the few-token tcgen05 kernels, block B the one-kernel decode
+    # block A runs the few-token tcgen05 kernels, block B the GEMV pair or the one-kernel decode
     assert fm.fmlp_mlp_gelu_plan(TA, DA, HA, DoA) == fm.FMLP_PLAN_TC
-    assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == fm.FMLP_PLAN_DECODE
+    assert fm.fmlp_mlp_gelu_plan(1, DB, HB, DoB) == \
+        (fm.FMLP_PLAN_DECODE if decode else fm.FMLP_PLAN_GEMV)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for _ in range(3):   # repeated, so that earlier blocks' kernels overlap later ones

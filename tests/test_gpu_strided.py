@@ -75,12 +75,15 @@ def _views(x, T, K, N, xpad, ypad):
 # T, D, H, extra columns left of x / of y, and the plan each size takes
 GEGLU_CASES = [(300, 64, 200, 8, 16, fm.FMLP_PLAN_FUSED_SMALL),
                (3, 768, 3072, 16, 8, fm.FMLP_PLAN_DECODE),
+               (1, 768, 3072, 16, 8, fm.FMLP_PLAN_GEMV),
                (40, 520, 1032, 8, 24, fm.FMLP_PLAN_TC),             # few-token kernels
                (700, 512, 1024, 32, 64, fm.FMLP_PLAN_TC)]           # batched tiles
 
 
 @pytest.mark.parametrize("T,D,H,xpad,ypad,plan", GEGLU_CASES)
-def test_geglu_on_column_slices(T, D, H, xpad, ypad, plan):
+def test_geglu_on_column_slices(T, D, H, xpad, ypad, plan, request):
+    if plan == fm.FMLP_PLAN_DECODE:
+        request.getfixturevalue("prefer_decode")
     assert fm.fmlp_geglu_plan(T, D, H) == plan
     x = bits((T, D), 2.0)
     Wg, Wu = bits((H, D), 1 / math.sqrt(D)), bits((H, D), 1 / math.sqrt(D))
@@ -99,12 +102,15 @@ def test_geglu_on_column_slices(T, D, H, xpad, ypad, plan):
 
 MLP_CASES = [(100, 40, 72, 48, 8, 16, fm.FMLP_PLAN_FUSED_SMALL),
              (1, 4096, 4096, 4096, 64, 128, fm.FMLP_PLAN_DECODE),
+             (1, 4096, 4096, 4096, 64, 128, fm.FMLP_PLAN_GEMV),
              (20, 1024, 2048, 520, 8, 8, fm.FMLP_PLAN_TC),
              (600, 384, 1040, 264, 16, 32, fm.FMLP_PLAN_TC)]
 
 
 @pytest.mark.parametrize("T,D,H,Do,xpad,ypad,plan", MLP_CASES)
-def test_mlp_on_column_slices(T, D, H, Do, xpad, ypad, plan):
+def test_mlp_on_column_slices(T, D, H, Do, xpad, ypad, plan, request):
+    if plan == fm.FMLP_PLAN_DECODE:
+        request.getfixturevalue("prefer_decode")
     assert fm.fmlp_mlp_gelu_plan(T, D, H, Do) == plan
     x = bits((T, D), 2.0)
     W1, b1 = bits((H, D), 1 / math.sqrt(D)), bits((H,), 1 / math.sqrt(D))

@@ -51,7 +51,7 @@ class DefaultPool:
         return v.value
 
 
-# a batched block (two tcgen05 kernels), the one-kernel decode at two tokens, ragged sizes
+# a batched block (two tcgen05 kernels), the GEMV pair at two tokens, ragged sizes
 @pytest.mark.parametrize("T,D,H", [(512, 768, 3072), (2, 768, 3072), (1000, 264, 1032)])
 def test_noalloc_matches_workspace_call_and_oracle_twice(T, D, H):
     fm.load()

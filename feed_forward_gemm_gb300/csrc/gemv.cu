@@ -11,17 +11,22 @@
 //     CTAs of 16 warps per SM;
 //   - the CTA's rows are cut into 512-byte segments (256 weights, one 16-byte vector per
 //     lane) and each warp takes one contiguous run of segments, so every warp streams its own
-//     contiguous range of W with 8 non-allocating 128-bit loads per lane in flight;
+//     contiguous range of W with 8 non-allocating 128-bit loads per lane in flight; each
+//     register, once its segment is summed, takes the load 8 segments ahead, so the
+//     arithmetic overlaps the stream instead of alternating with it;
 //   - programmatic dependent launch: the kernel lets the next kernel launch at once; after
 //     waiting for the previous kernel, the first batch of weight loads is issued before x is
-//     staged, so the x load hides under them. (L2 prefetches of the CTA's own rows, or of the
-//     next layer's weights, were measured to slow the decode forward down: they queue ahead
-//     of the loads the warps need first.)
-//   - x (T x K bf16) sits in shared memory; each lane accumulates its dot products in fp32
-//     across the consecutive segments of one row and the warp reduces with shuffles only when
-//     its run crosses a row boundary. The reduced sum of a run piece is stored as the partial
-//     of the piece's first segment (the piece's other segments get 0), and one thread per
-//     (row, token) adds a row's partials in segment order: deterministic for a given shape;
+//     staged, so the x load hides under them. (Requesting x first, L2 prefetches of the CTA's
+//     own rows, of the next layer's weights, or before the dependency wait, and one CTA per SM
+//     so the next kernel can be resident early, were all measured slower.)
+//   - x (T x K) sits in shared memory, widened to fp32 when that still leaves room for two
+//     CTAs per SM; each lane accumulates its dot products in fp32 (packed f32x2
+//     multiply-adds) across the consecutive segments of one row and the warp reduces with
+//     shuffles only when its run crosses a row boundary, storing the piece's sum as the
+//     partial of (row, warp). A row's 16 partials are then added by a butterfly in a fixed
+//     order: deterministic for a given shape. The (matrix, row, segment) cursor advances by
+//     additions: a division by the run-time segment count per segment cost more instructions
+//     than the multiply-adds;
 //   - with two weight matrices (GeGLU gate and up) both blocks are streamed and the epilogue
 //     forms gelu_tanh(g) * u.
 #include "activation.cuh"
@@ -84,44 +89,46 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   const int total = NMAT * per_mat;          // segments this CTA streams
   const int C = K / 8;
   const size_t xbytes = static_cast<size_t>(T) * K * (XF32 ? 4 : 2);
-  float* part = reinterpret_cast<float*>(gsm + xbytes);  // [seg][T]
+  // partial sums, one per (matrix, row, warp, token): a warp's run of segments covers at most
+  // one contiguous piece of each row
+  float* part = reinterpret_cast<float*>(gsm + xbytes);
   const uint32_t xs = smem_u32(gsm);
 
   // warp w streams segments [g0, g1) of the CTA's list (matrix-major, then row, then segment)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g0 = static_cast<int>((static_cast<int64_t>(warp) * total) / kGemvWarps);
   const int g1 = static_cast<int>((static_cast<int64_t>(warp + 1) * total) / kGemvWarps);
-  uint4 wv[kGemvBatch];
-  auto load_batch = [&](int base) {
-#pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int g = base + u;
-      if (g < g1) {
-        const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
-        const int gm = g - mat * per_mat;
-        const __nv_bfloat16* Wm = mat ? W1 : W0;
-        // consecutive segments of a matrix block are consecutive 512-byte pieces of memory
-        wv[u] = ld_stream_v4(Wm + static_cast<size_t>(r0) * K + static_cast<size_t>(gm) * kSeg +
-                             lane * 8);
-      } else {
-        wv[u] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+  // this lane's 16 bytes of segment g (consecutive segments of a matrix block are consecutive
+  // 512-byte pieces of memory)
+  auto load_seg = [&](int g) {
+    const int mat = NMAT == 2 ? (g >= per_mat ? 1 : 0) : 0;
+    const int gm = g - mat * per_mat;
+    const __nv_bfloat16* Wm = mat ? W1 : W0;
+    return ld_stream_v4(Wm + static_cast<size_t>(r0) * K + static_cast<size_t>(gm) * kSeg +
+                        lane * 8);
   };
-  load_batch(g0);   // in flight while x is staged
-
-  // x rows are ldx elements apart (a multiple of 8)
-  for (int i = threadIdx.x; i < T * C; i += kGemvThreads) {
-    const int t = i / C, c = i - t * C;
-    const uint4 v = ld_cg_v4(x + static_cast<size_t>(t) * ldx + static_cast<size_t>(c) * 8);
+  auto stage_x = [&](int i, uint4 v) {
     if (XF32) {
+      const int t = i / C, c = i - t * C;
       float4* xf = reinterpret_cast<float4*>(gsm);
       xf[t * 2 * C + c] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
       xf[t * 2 * C + C + c] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     } else {
       reinterpret_cast<uint4*>(gsm)[i] = v;
     }
-  }
+  };
+  auto x_at = [&](int i) {   // x rows are ldx elements apart (a multiple of 8)
+    const int t = i / C, c = i - t * C;
+    return ld_cg_v4(x + static_cast<size_t>(t) * ldx + static_cast<size_t>(c) * 8);
+  };
+  // the first weights go out before x is requested (x first was measured slower: it holds
+  // back the weight stream)
+  uint4 wv[kGemvBatch];
+#pragma unroll
+  for (int u = 0; u < kGemvBatch; ++u)
+    wv[u] = g0 + u < g1 ? load_seg(g0 + u) : make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < T * C; i += kGemvThreads) stage_x(i, x_at(i));
+  for (int i = threadIdx.x; i < NMAT * rows * kGemvWarps * T; i += kGemvThreads) part[i] = 0.f;
   __syncthreads();
 
   // cursor of the segment being summed: matrix, row, segment within the row
@@ -141,7 +148,6 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
 #pragma unroll
     for (int k = 0; k < NA; ++k) acc[t][k] = make_float2(0.f, 0.f);
   int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
-  int piece_pi = 0;     // its partial index
   auto flush = [&]() {
     float v[TMAX];
 #pragma unroll
@@ -156,25 +162,18 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
     if (lane == 0) {
 #pragma unroll
       for (int t = 0; t < TMAX; ++t)
-        if (t < T) part[piece_pi + t] = v[t];
+        if (t < T) part[(piece_row * kGemvWarps + warp) * T + t] = v[t];
     }
   };
   for (int base = g0; base < g1; base += kGemvBatch) {
-    if (base != g0) load_batch(base);
 #pragma unroll
     for (int u = 0; u < kGemvBatch; ++u) {
       const int g = base + u;
       if (g >= g1) break;  // warp-uniform
       const int rid = cmat * rows + crow;
-      const int pi = g * T;
       if (rid != piece_row) {
         if (piece_row >= 0) flush();
         piece_row = rid;
-        piece_pi = pi;
-      } else if (lane == 0) {
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t)
-          if (t < T) part[pi + t] = 0.f;
       }
       const uint32_t chunk = static_cast<uint32_t>(cseg * (kSeg / 8) + lane);
 #pragma unroll
@@ -194,6 +193,9 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
           dot8x2(acc[t][u % NA], wv[u], xa, xb);
         }
       }
+      // the register just used takes the load kGemvBatch segments ahead, so that the
+      // arithmetic overlaps the stream (about kGemvBatch loads per lane stay in flight)
+      if (g + kGemvBatch < g1) wv[u] = load_seg(g + kGemvBatch);
       // advance the cursor
       if (++cseg == segs) {
         cseg = 0;
@@ -207,14 +209,13 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   if (piece_row >= 0) flush();
   __syncthreads();
 
-  // one warp per (row, token): the lanes add the row's segment partials (lane l takes segments
-  // l, l + 32, ...; a fixed order: deterministic), then the epilogue
+  // one warp per (row, token): lanes 0..15 take the 16 warps' partials of the row, summed by
+  // a butterfly (a fixed order: deterministic), then the epilogue
   for (int i = warp; i < rows * T; i += kGemvWarps) {
     const int row = i / T, t = i - row * T;
-    float s0 = 0.f, s1 = 0.f;
-    for (int sg = lane; sg < segs; sg += 32) s0 += part[(row * segs + sg) * T + t];
-    if (NMAT == 2)
-      for (int sg = lane; sg < segs; sg += 32) s1 += part[(per_mat + row * segs + sg) * T + t];
+    float s0 = lane < kGemvWarps ? part[(row * kGemvWarps + lane) * T + t] : 0.f;
+    float s1 = 0.f;
+    if (NMAT == 2 && lane < kGemvWarps) s1 = part[((rows + row) * kGemvWarps + lane) * T + t];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       s0 += __shfl_xor_sync(0xffffffffu, s0, o);
@@ -253,10 +254,11 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
                                    r1);
 }
 
-// Row partials of the CTA (its rows x segments x tokens, fp32).
+// Row partials of the CTA (its rows x 16 warps x tokens, fp32).
 static size_t gemv_part_bytes(int T, int K, int N, int nmat, int grid) {
+  (void)K;
   const int64_t rows_max = (static_cast<int64_t>(N) + grid - 1) / grid;
-  return static_cast<size_t>(nmat) * rows_max * (K / kSeg) * T * 4;
+  return static_cast<size_t>(nmat) * rows_max * kGemvWarps * T * 4;
 }
 
 // x is kept as fp32 while the CTA's shared memory stays within this (two CTAs per SM fit).

@@ -50,6 +50,8 @@ struct DeviceState {
   int sms = 0;
   int major = 0, minor = 0;
   int max_pairs = 0;   // co-resident CTA pairs of the pair GEMM (0: pair kernel unavailable)
+  // co-resident clusters of 1, 2, 4, 8 few-token CTAs (0: unknown, assume sms / size)
+  int skinny_clusters[4] = {0, 0, 0, 0};
   int* status = nullptr;
   int decode_occ = 0;  // resident decode CTAs per SM (0: the one-kernel decode cannot run)
   unsigned long long* decode_bar = nullptr;  // grid-barrier counters (kDecodeSlots)
@@ -137,6 +139,12 @@ fmlp_status device_state(DeviceState** out) {
     if (gemm_tc2_max_pairs(&d.max_pairs) != cudaSuccess) {
       d.max_pairs = 0;
       (void)cudaGetLastError();
+    }
+    for (int i = 0; i < 4; ++i) {
+      if (gemm_skinny_max_clusters(1 << i, &d.skinny_clusters[i]) != cudaSuccess) {
+        d.skinny_clusters[i] = 0;
+        (void)cudaGetLastError();
+      }
     }
     if (decode_occupancy(&d.decode_occ) != cudaSuccess ||
         decode_barrier_base(&d.decode_bar) != cudaSuccess) {
@@ -428,13 +436,35 @@ bool use_skinny(int64_t M) {
          g_tile_policy.load(std::memory_order_relaxed) == FMLP_TILES_AUTO;
 }
 
-// K slices per 128-row weight tile: the largest power of two <= 8 that keeps tiles * S within
-// the SM count and gives every slice at least one 64-deep K step.
-int skinny_split(const DeviceState& d, int64_t N_out, int64_t K) {
-  const int64_t tiles = (N_out + 127) / 128, num_kb = (K + 63) / 64;
-  int S = 1;
-  while (S < 8 && tiles * S * 2 <= d.sms && S * 2 <= num_kb) S *= 2;
-  return S;
+// Tiling of the few-token kernel: K slices S (a power of two <= 8, every slice at least one
+// 64-deep K step) and weight rows per tile R (a multiple of 4, at most 128), all tiles * S
+// CTAs in one wave (one CTA per SM; the tiles may not outnumber the clusters of S CTAs that
+// fit at once, which the GPCs decide, not just the SM count). Each CTA moves (R + Tpad) rows
+// of K / S elements through its TMA (its weight rows and the tokens, which every tile reads
+// again), so the choice minimises (R + Tpad) / S: more, shorter tiles put more SMs to work
+// but re-read x more often (56-row tiles on 148 SMs ran slower than 128-row ones on 128).
+struct SkinnyShape {
+  int rows, tiles, split;
+};
+
+SkinnyShape skinny_shape(const DeviceState& d, int64_t N_out, int64_t K, int64_t tpad) {
+  const int64_t num_kb = (K + 63) / 64;
+  SkinnyShape best{128, static_cast<int>((N_out + 127) / 128), 1};
+  double best_cost = -1.0;
+  for (int S = 1, i = 0; S <= 8 && S <= num_kb; S *= 2, ++i) {
+    const int64_t tiles_max = d.skinny_clusters[i] > 0 ? d.skinny_clusters[i] : d.sms / S;
+    if (tiles_max < 1) break;
+    int64_t R = (N_out + tiles_max - 1) / tiles_max;
+    R = (R + 3) / 4 * 4;
+    if (R > 128) continue;              // 128-row tiles would not fit in one wave
+    const int64_t tiles = (N_out + R - 1) / R;
+    const double cost = static_cast<double>(R + tpad) / S;
+    if (best_cost < 0.0 || cost < best_cost) {
+      best = SkinnyShape{static_cast<int>(R), static_cast<int>(tiles), S};
+      best_cost = cost;
+    }
+  }
+  return best;                          // no fit: 128-row tiles, no K split
 }
 
 fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const void* B0,
@@ -445,9 +475,10 @@ fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const vo
   SkinnyLaunch L;
   memset(&L, 0, sizeof L);
   L.tpad = static_cast<int>((M + 31) / 32 * 32);
-  FMLP_TRY(make_map(&L.tmW0, B0, N_out, K, 128, "W"));
+  const SkinnyShape sh = skinny_shape(d, N_out, K, L.tpad);
+  FMLP_TRY(make_map(&L.tmW0, B0, N_out, K, static_cast<uint32_t>(sh.rows), "W"));
   if (epi == EPI_GEGLU) {
-    FMLP_TRY(make_map(&L.tmW1, B1, N_out, K, 128, "W_up"));
+    FMLP_TRY(make_map(&L.tmW1, B1, N_out, K, static_cast<uint32_t>(sh.rows), "W_up"));
   } else {
     L.tmW1 = L.tmW0;
   }
@@ -458,8 +489,9 @@ fmlp_status launch_skinny(const DeviceState& d, int epi, const void* A, const vo
   L.N = static_cast<int>(N_out);
   L.K = static_cast<int>(K);
   L.ldy = static_cast<int>(ldy > 0 ? ldy : N_out);
-  L.tiles = static_cast<int>((N_out + 127) / 128);
-  L.split = skinny_split(d, N_out, K);
+  L.rows = sh.rows;
+  L.tiles = sh.tiles;
+  L.split = sh.split;
   L.epi = epi;
   L.gelu_mode = gelu_mode;
   L.pdl = pdl;
@@ -1143,13 +1175,14 @@ fmlp_status fmlp_mlp_gelu_strided(const void* x, int64_t ldx, const void* W1, co
 static std::string describe_gemm(const DeviceState& d, const char* name, int epi, int64_t M,
                                  int64_t N, int64_t K) {
   if (use_skinny(M)) {
+    const SkinnyShape sh = skinny_shape(d, N, K, (M + 31) / 32 * 32);
     char b[256];
     snprintf(b, sizeof b,
-             "%s: tcgen05 few-token kernel, 128 weight rows x %lld tokens per tile, K split %d "
+             "%s: tcgen05 few-token kernel, %d weight rows x %lld tokens per tile, K split %d "
              "ways over a cluster, M=%lld N=%lld K=%lld, grid=%lld",
-             name, static_cast<long long>((M + 31) / 32 * 32), skinny_split(d, N, K),
+             name, sh.rows, static_cast<long long>((M + 31) / 32 * 32), sh.split,
              static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-             static_cast<long long>((N + 127) / 128 * skinny_split(d, N, K)));
+             static_cast<long long>(sh.tiles) * sh.split);
     return b;
   }
   const GemmChoice c = choose_gemm(d, epi, M, N);

@@ -9,13 +9,23 @@
 //     nn.Linear layout as stored), B = the T tokens padded to Tpad (a multiple of 32, rows past
 //     T read as zeros by TMA), M = 128, N = Tpad, K = 16 per instruction; every byte of each
 //     16 KB A stage is a weight;
-//   - a 128-row weight tile is cut into S K slices (S = 1, 2, 4 or 8) computed by the S CTAs
-//     of one thread-block cluster, so tiles * S CTAs stream the weights at once;
-//   - each CTA parks its fp32 slice D_s[128 x Tpad] in its own shared memory (the stage ring,
-//     no longer needed), the cluster synchronises, and CTA r adds rows [r*128/S, (r+1)*128/S)
-//     of all S slices read through distributed shared memory in slice order s = 0..S-1 (the
-//     same order on every run), applies the epilogue (bias, GELU/ReLU, or gelu_tanh(g)*u for
-//     the GeGLU gate/up pair, whose two accumulators share the B tile) and writes y[t, n].
+//   - a weight tile of R rows (R <= 128, a multiple of 4) is cut into S K slices (S = 1, 2, 4
+//     or 8) computed by the S CTAs of one thread-block cluster, so tiles * S CTAs stream the
+//     weights at once. R is chosen so that tiles * S fills the SMs: a 4096-row layer takes 38
+//     tiles of 108 rows x 4 slices = 152 CTAs, where 128-row tiles left 24 of 152 SMs idle.
+//     TMA loads R rows; the MMA still runs M = 128, and its rows past R (whatever shared
+//     memory follows the tile) are never read back;
+//   - CTA r owns rows [r rr, (r+1) rr) of the tile's R (rr = R / S rounded up to 4). Once
+//     every CTA of the cluster has finished its MMAs (a cluster barrier: every stage ring is
+//     free), each CTA reads its fp32 slice D_s out of TMEM and pushes each row's T token
+//     values straight into the owning CTA's ring with distributed-shared-memory stores
+//     (fire-and-forget; only the T real tokens, not the padding); after a second cluster
+//     barrier the owner adds the S slices of its rows from its own shared memory in slice
+//     order s = 0..S-1 (the same order on every run), applies the epilogue (bias, GELU/ReLU,
+//     or gelu_tanh(g)*u for the GeGLU gate/up pair, whose two accumulators share the B tile)
+//     and writes y[t, n]. (Copying the slice to the CTA's own shared memory and pulling the S
+//     slices with remote loads instead took 1 us at 4 tokens and 3.5 us at 128: those loads
+//     wait a full round trip each.)
 // No global scratch, no atomics, no CTA waiting on another outside the cluster barrier,
 // which the hardware provides (the CTAs of a cluster are co-scheduled).
 //
@@ -36,20 +46,23 @@ constexpr int kSkBK = 64;                   // K per stage: one 128-byte swizzle
 constexpr int kSkRows = 128;                // weight rows per tile (MMA M)
 constexpr int kSkA = kSkRows * kSkBK * 2;   // 16 KB of weights per matrix per stage
 
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+__device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 lds_f4_local(uint32_t addr) {
   float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
+               : "r"(addr)
                : "memory");
   return v;
 }
 
 template <int EPI>
-__device__ __forceinline__ float skinny_out(float a0, float a1, const __nv_bfloat16* bias, int n,
-                                            int gelu_mode) {
+__device__ __forceinline__ float skinny_out(float a0, float a1, float b, int gelu_mode) {
   if (EPI == EPI_GEGLU) return gelu_tanh_f(a0) * a1;
-  const float z = a0 + (bias != nullptr ? __bfloat162float(bias[n]) : 0.f);
+  const float z = a0 + b;
   return EPI == EPI_BIAS_GELU ? gelu_f(z, gelu_mode) : z;
 }
 
@@ -62,7 +75,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                        const __grid_constant__ CUtensorMap tmW1,
                        const __grid_constant__ CUtensorMap tmX,
                        const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ y,
-                       int T, int N, int K, int ldy, int Tpad, int stages, int gelu_mode,
+                       int T, int N, int K, int ldy, int Tpad, int R, int stages, int gelu_mode,
                        int* status, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -73,14 +86,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint64_t* empty = full + stages;
   uint64_t* tfull = empty + stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
-  // after the main loop the ring holds this CTA's slice: [mat][t][128 rows] fp32
+  // this CTA's rows of the bias (at most 128), fetched while the weights stream
+  float* bias_s = reinterpret_cast<float*>(tmem_slot + 4);
+  // after the main loop the ring receives the slices of this CTA's rows: [S][mat][Tpad][rr] fp32
   float* part = reinterpret_cast<float*>(ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = static_cast<int>(cluster_nctarank());   // K slices of the tile
   const int s = static_cast<int>(cluster_ctarank());
   const int tile = blockIdx.x / S;
-  const int n0 = tile * kSkRows;
+  const int n0 = tile * R;
+  // bytes one stage receives: R rows of each weight matrix and the Tpad token rows
+  const uint32_t tx_bytes = static_cast<uint32_t>(NMAT * R * kSkBK * 2 + b_bytes);
   const int num_kb = (K + kSkBK - 1) / kSkBK;
   const int kb0 = s * num_kb / S, kb1 = (s + 1) * num_kb / S;
   const uint32_t tmem_cols = NMAT * Tpad <= 32 ? 32u : (NMAT * Tpad <= 64 ? 64u
@@ -109,15 +126,17 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   pdl_wait_primary();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
+  bool tfull_ok = true;   // the epilogue warps' wait for the accumulators
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      int kb = kb0;
+      for (; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, status, SITE_PRODUCER_EMPTY, timeout_ns)) break;
         uint8_t* st = ring + stage * stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
+        mbar_arrive_expect_tx(&full[stage], tx_bytes);
         tma_load_2d(st, &tmW0, &full[stage], kb * kSkBK, n0);
         if (NMAT == 2) tma_load_2d(st + kSkA, &tmW1, &full[stage], kb * kSkBK, n0);
         tma_load_2d(st + NMAT * kSkA, &tmX, &full[stage], kb * kSkBK, 0);
@@ -157,54 +176,73 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ TMEM -> shared memory
-    const int wq = warp & 3;   // this warp may read TMEM lanes [32 wq, 32 wq + 32)
-    const bool ok = mbar_wait(tfull, 0, status, SITE_EPI_TMEM_FULL, timeout_ns);
+    // ------------------------------------------------------------------ epilogue warps
+    // the bias of the rows this CTA finishes, while the weights stream (read in the tail it
+    // cost a full memory round trip per output)
+    if (EPI != EPI_GEGLU) {
+      const int rr = (R + 4 * S - 1) / (4 * S) * 4;
+      for (int i = threadIdx.x - 64; i < rr; i += kSkThreads - 64) {
+        const int n = n0 + s * rr + i;
+        bias_s[i] = (bias != nullptr && s * rr + i < R && n < N) ? __bfloat162float(bias[n]) : 0.f;
+      }
+    }
+    tfull_ok = mbar_wait(tfull, 0, status, SITE_EPI_TMEM_FULL, timeout_ns);
     __syncwarp();
     tc_fence_after();
-    if (__all_sync(0xffffffffu, ok)) {
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
-      const int row = wq * 32 + lane;
-      for (int mat = 0; mat < NMAT; ++mat) {
-        for (int c = 0; c < Tpad; c += 32) {
-          uint32_t a[32];
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(mat * Tpad + c), a);
-          tmem_ld_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // every CTA's MMAs are done: every stage ring may take the slices
+
+  // ------------------------------------------------------------------ push the slices
+  // Slice s of row `row` goes to the owner of the row, into its ring at
+  // recv[s][mat][t][lr] (lr = row - owner rr): [S][NMAT][Tpad][rr] fp32. Rows are contiguous,
+  // so a warp's 32 rows go out as 128 contiguous bytes per token (16-byte vectors per thread,
+  // tokens contiguous, were slower: a warp's lanes then hit one shared-memory bank).
+  const int rr = (R + 4 * S - 1) / (4 * S) * 4;
+  const uint32_t recv_addr = smem_u32(part);
+  if (warp >= 2 && __all_sync(0xffffffffu, tfull_ok)) {
+    const int wq = warp & 3;   // this warp may read TMEM lanes [32 wq, 32 wq + 32)
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+    const int row = wq * 32 + lane;
+    const int owner = row < R ? row / rr : 0;
+    const int lr = row - owner * rr;
+    const uint32_t dst0 = mapa_shared(recv_addr, static_cast<uint32_t>(owner));
+    for (int mat = 0; mat < NMAT; ++mat) {
+      for (int c = 0; c < T; c += 32) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(mat * Tpad + c), a);
+        tmem_ld_wait();
+        if (row < R) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            part[(static_cast<size_t>(mat) * Tpad + c + j) * kSkRows + row] = __uint_as_float(a[j]);
+          for (int j = 0; j < 32; ++j) {
+            if (c + j < T) {
+              const int idx = ((s * NMAT + mat) * Tpad + c + j) * rr + lr;
+              st_dsmem_f32(dst0 + static_cast<uint32_t>(idx) * 4u, __uint_as_float(a[j]));
+            }
+          }
         }
       }
     }
   }
   tc_fence_before();
-  __syncthreads();
-  cluster_sync();   // every slice of the tile is in its CTA's shared memory
+  cluster_sync();   // every slice is in its owner's shared memory
 
-  // ------------------------------------------------------------------ cluster reduction
-  // CTA s finishes rows [s * rr, (s + 1) * rr) of the tile for every token, four consecutive
-  // rows per thread: all S slices of the four rows (16-byte distributed-shared-memory loads,
-  // every slice in flight at once) are added in slice order q = 0..S-1, the same order for
-  // every element and every run. Consecutive threads take consecutive row groups, so the
-  // writes of y[t, n0 + row .. + 3] are contiguous 8-byte stores.
+  // ------------------------------------------------------------------ owner reduction
+  // CTA s finishes its rows for every token, four consecutive rows per thread: the S slices
+  // of the four rows (16-byte loads from this CTA's own shared memory) are added in slice
+  // order q = 0..S-1, the same order for every element and every run. Consecutive threads
+  // take consecutive row groups, so the writes of y[t, n0 + row .. + 3] are contiguous
+  // 8-byte stores.
   {
-    const int rr = kSkRows / S;
-    const int rg = rr / 4;
-    const uint32_t part_addr = smem_u32(part);
+    const int r_lo = s * rr < R ? s * rr : R;
+    const int r_hi = r_lo + rr < R ? r_lo + rr : R;
+    const int rg = (r_hi - r_lo) / 4;   // R is a multiple of 4
     for (int e = threadIdx.x; e < rg * T; e += kSkThreads) {
       const int t = e / rg;
-      const int row = s * rr + (e - t * rg) * 4;
-      const int n = n0 + row;
+      const int lr = (e - t * rg) * 4;
+      const int n = n0 + r_lo + lr;
       if (n >= N) continue;
-      float4 q4[NMAT][8];
-#pragma unroll
-      for (int mat = 0; mat < NMAT; ++mat) {
-        const uint32_t off = static_cast<uint32_t>(((mat * Tpad + t) * kSkRows + row) *
-                                                   static_cast<int>(sizeof(float)));
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < S) q4[mat][q] = ld_dsmem_v4(mapa_shared(part_addr + off, static_cast<uint32_t>(q)));
-      }
       float4 acc[NMAT];
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
@@ -212,17 +250,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (q < S) {
-            acc[mat].x += q4[mat][q].x;
-            acc[mat].y += q4[mat][q].y;
-            acc[mat].z += q4[mat][q].z;
-            acc[mat].w += q4[mat][q].w;
+            const int idx = ((q * NMAT + mat) * Tpad + t) * rr + lr;
+            const float4 v = lds_f4_local(recv_addr + static_cast<uint32_t>(idx) * 4u);
+            acc[mat].x += v.x;
+            acc[mat].y += v.y;
+            acc[mat].z += v.z;
+            acc[mat].w += v.w;
           }
         }
       }
-      const float o0 = skinny_out<EPI>(acc[0].x, acc[NMAT - 1].x, bias, n, gelu_mode);
-      const float o1 = skinny_out<EPI>(acc[0].y, acc[NMAT - 1].y, bias, n + 1, gelu_mode);
-      const float o2 = skinny_out<EPI>(acc[0].z, acc[NMAT - 1].z, bias, n + 2, gelu_mode);
-      const float o3 = skinny_out<EPI>(acc[0].w, acc[NMAT - 1].w, bias, n + 3, gelu_mode);
+      const bool epb = EPI != EPI_GEGLU;
+      const float o0 = skinny_out<EPI>(acc[0].x, acc[NMAT - 1].x, epb ? bias_s[lr] : 0.f, gelu_mode);
+      const float o1 = skinny_out<EPI>(acc[0].y, acc[NMAT - 1].y, epb ? bias_s[lr + 1] : 0.f, gelu_mode);
+      const float o2 = skinny_out<EPI>(acc[0].z, acc[NMAT - 1].z, epb ? bias_s[lr + 2] : 0.f, gelu_mode);
+      const float o3 = skinny_out<EPI>(acc[0].w, acc[NMAT - 1].w, epb ? bias_s[lr + 3] : 0.f, gelu_mode);
       __nv_bfloat16* yr = y + static_cast<size_t>(t) * ldy + n;
       if (n + 3 < N) {
         uint2 pk;
@@ -236,26 +277,31 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       }
     }
   }
-  cluster_sync();   // no CTA leaves while another may still read its shared memory
+  // no other CTA touches this one's shared memory after the second barrier: no third one
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
   }
 }
 
-// Shared memory of one CTA: the stage ring (also the slice buffer afterwards), the mbarriers
-// and the TMEM address slot, plus 1 KB for the 1024-byte alignment of the ring.
+// Shared memory of one CTA: the stage ring (also the slice buffer afterwards), the mbarriers,
+// the TMEM address slot and the bias of up to 128 rows, plus 1 KB for the 1024-byte alignment
+// of the ring.
 static int skinny_smem(int nmat, int tpad, int stages) {
   const int stage_bytes = nmat * kSkA + tpad * kSkBK * 2;
-  return 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
+  return 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16 + 128 * 4;
 }
 
-// Pipeline stages for nmat weight matrices and tpad token rows (0: does not fit).
+// Pipeline stages for nmat weight matrices and tpad token rows (0: does not fit): up to 192 KB
+// of ring. (A ring of about 100 KB, which leaves room for the next kernel's CTA on the SM so
+// that it can fetch its weights before the dependency wait, measured slower: 24.2 and 29.5 us
+// against 23.3 and 26.6 for the 4096-wide MLP at 64 and 128 tokens; fetching the weights
+// early with the full ring was slower too.) The ring must also take the slices of a CTA's
+// rows, [S][nmat][tpad][rr] fp32 with S rr <= 128.
 static int gemm_skinny_stages(int nmat, int tpad) {
   const int stage_bytes = nmat * kSkA + tpad * kSkBK * 2;
   int stages = (192 * 1024) / stage_bytes;
   if (stages > 8) stages = 8;
-  // the ring must also hold the fp32 slice [nmat][tpad][128]
   while (stages * stage_bytes < nmat * tpad * kSkRows * 4) ++stages;
   return skinny_smem(nmat, tpad, stages) <= 232448 ? stages : 0;
 }
@@ -285,15 +331,37 @@ static cudaError_t launch_skinny_t(const SkinnyLaunch& L) {
   cfg.numAttrs = L.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, L.tmW0, L.tmW1, L.tmX,
                             static_cast<const __nv_bfloat16*>(L.bias),
-                            static_cast<__nv_bfloat16*>(L.y), L.T, L.N, L.K, L.ldy, L.tpad, stages,
-                            L.gelu_mode, L.status, L.timeout_ns);
+                            static_cast<__nv_bfloat16*>(L.y), L.T, L.N, L.K, L.ldy, L.tpad, L.rows,
+                            stages, L.gelu_mode, L.status, L.timeout_ns);
+}
+
+cudaError_t gemm_skinny_max_clusters(int split, int* clusters) {
+  auto kern = gemm_skinny_kernel<EPI_BIAS, 1>;
+  // one CTA per SM (a launch never uses more: the second CTA slot is for the next kernel)
+  const int smem = 200 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, 1, 1);
+  cfg.blockDim = dim3(kSkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
 cudaError_t gemm_skinny_launch(const SkinnyLaunch& L) {
   const int num_kb = (L.K + kSkBK - 1) / kSkBK;
   if (L.T < 1 || L.T > kSkinnyMaxT || L.tpad < L.T || L.tpad % 32 != 0 || L.tpad > kSkinnyMaxT ||
-      L.tiles < 1 || (L.split != 1 && L.split != 2 && L.split != 4 && L.split != 8) ||
-      L.split > num_kb)
+      L.rows < 4 || L.rows > kSkRows || L.rows % 4 != 0 ||
+      L.tiles < 1 || static_cast<int64_t>(L.tiles) * L.rows < L.N ||
+      (L.split != 1 && L.split != 2 && L.split != 4 && L.split != 8) || L.split > num_kb)
     return cudaErrorInvalidValue;
   switch (L.epi) {
     case EPI_BIAS: return launch_skinny_t<EPI_BIAS, 1>(L);

@@ -70,7 +70,7 @@ constexpr int kMoeMaxExperts = 256;
 // Few-token tcgen05 GEMM (weights as the MMA's M side, K split over a cluster; gemm_skinny.cu).
 constexpr int kSkinnyMaxT = 128;
 struct SkinnyLaunch {
-  CUtensorMap tmW0;   // weights [N, K] bf16, box {64, 128}, 128B swizzle (Wg for GeGLU)
+  CUtensorMap tmW0;   // weights [N, K] bf16, box {64, rows}, 128B swizzle (Wg for GeGLU)
   CUtensorMap tmW1;   // Wu for GeGLU (else a copy of tmW0)
   CUtensorMap tmX;    // x [T, K] bf16, box {64, tpad}, 128B swizzle
   const void* bias;   // [N] or nullptr
@@ -78,15 +78,19 @@ struct SkinnyLaunch {
   int T, N, K;
   int ldy;            // row stride of y in elements
   int tpad;           // T rounded up to a multiple of 32 (the MMA's N)
-  int tiles;          // ceil(N / 128)
+  int rows;           // weight rows per tile: a multiple of 4, at most 128 (the MMA's M)
+  int tiles;          // ceil(N / rows)
   int split;          // K slices per tile = cluster size: 1, 2, 4 or 8
   int epi, gelu_mode;
-  bool pdl;
+  bool pdl;           // programmatic dependent launch (second kernel of a block call)
   cudaStream_t stream;
   int* status;
   uint64_t timeout_ns;
 };
 cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
+// Clusters of `split` few-token CTAs that can be resident at once (the GPCs decide how many
+// clusters of a size fit, not just the SM count).
+cudaError_t gemm_skinny_max_clusters(int split, int* clusters);
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
 // The single-SM kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).

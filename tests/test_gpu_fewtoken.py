@@ -1,7 +1,7 @@
 """The few-token tcgen05 kernel (T <= 128 tokens: the weights are the MMA's M side and each
-128-row weight tile is split along K over a cluster of 1, 2, 4 or 8 CTAs, which add their
-slices through distributed shared memory) against the oracle: ragged T, N and K, every
-epilogue, every split size, and the same bits from call to call."""
+weight tile of up to 128 rows is split along K over a cluster of 1, 2, 4 or 8 CTAs, which
+add their slices through distributed shared memory) against the oracle: ragged T, N and K,
+partial tiles, every epilogue, the tiling rules, and the same bits from call to call."""
 import math
 
 import numpy as np
@@ -26,16 +26,20 @@ def ubits(shape, bound):
     return rne_bf16_array(rng.uniform(-bound, bound, shape))
 
 
-def split_of(text):
-    return int(text.split("K split ")[1].split(" ")[0])
+def tiling_of(text):
+    """(weight rows per tile, K split, grid) from a few-token plan description."""
+    rows = int(text.split(" weight rows")[0].split(", ")[-1])
+    split = int(text.split("K split ")[1].split(" ")[0])
+    grid = int(text.split("grid=")[1].split()[0].rstrip(","))
+    return rows, split, grid
 
 
-# T, K, N and the K split the sizes lead to on a 152-SM GB300: 2 tiles of N, 17 K steps
-# (8 slices); 32 tiles (4); 8 tiles of 2 K steps (2); 224 tiles (1, more tiles than SMs);
-# K = 8, a single partial K step (1); one token with K not a multiple of 256 (no GEMV, 8);
-# 7 tiles of 10 K steps (8)
-LINEAR_CASES = [(33, 1032, 136, 8), (5, 4096, 4096, 4), (100, 72, 1000, 2),
-                (128, 256, 28672, 1), (64, 8, 64, 1), (1, 4104, 520, 8), (97, 640, 776, 8)]
+# T, K, N and the K split where the sizes force it: 128-row tiles already outnumber the SMs
+# (no split), a single partial K step (none), two K steps (at most 2); the others (2 tiles of
+# N over 17 K steps, the 4096-wide layer, one token with K not a multiple of 256, 7 tiles of
+# 10 K steps) take whatever split fills the most SMs in one wave
+LINEAR_CASES = [(33, 1032, 136, None), (5, 4096, 4096, None), (100, 72, 1000, 2),
+                (128, 256, 28672, 1), (64, 8, 64, 1), (1, 4104, 520, None), (97, 640, 776, None)]
 
 
 @pytest.mark.parametrize("T,K,N,split", LINEAR_CASES)
@@ -43,7 +47,13 @@ LINEAR_CASES = [(33, 1032, 136, 8), (5, 4096, 4096, 4), (100, 72, 1000, 2),
 def test_fewtoken_linear_vs_oracle(T, K, N, split, with_bias):
     text = fm.fmlp_describe_plan("linear", T, K, N)
     assert "few-token" in text, text
-    assert split_of(text) == split, text
+    rows, S, grid = tiling_of(text)
+    assert rows % 4 == 0 and 4 <= rows <= 128 and S in (1, 2, 4, 8), text
+    assert grid == -(-N // rows) * S and S <= -(-K // 64), text
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert grid <= sms or (rows == 128 and S == 1), text     # one wave
+    if split is not None:
+        assert S == split, text
     x, W = rbits((T, K)), ubits((N, K), 1 / math.sqrt(K))
     b = ubits((N,), 1 / math.sqrt(K)) if with_bias else None
     _, y, check = guarded_bf16(T, N)
@@ -51,6 +61,13 @@ def test_fewtoken_linear_vs_oracle(T, K, N, split, with_bias):
     torch.cuda.synchronize()
     check()
     assert_parity(to_host(y), oracle.linear(x, W, b), f"few-token linear {T}x{K}->{N}")
+
+
+def test_fewtoken_4096_layer_fills_more_sms_than_128_row_tiles():
+    """The 4096-row layer: partial tiles (fewer than 128 weight rows) let more CTAs stream
+    than the 32 x 4 = 128 of full 128-row tiles."""
+    rows, S, grid = tiling_of(fm.fmlp_describe_plan("linear", 16, 4096, 4096))
+    assert grid > 128 or rows == 128, (rows, S, grid)
 
 
 @pytest.mark.parametrize("mode", [fm.FMLP_GELU_TANH, fm.FMLP_GELU_ERF, fm.FMLP_RELU])

@@ -43,7 +43,8 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="headline only")
     p.add_argument("--cpu-sample-rows", type=int, default=0)
     p.add_argument("--profile-kernel", default=None,
-                   choices=["gate_up", "down", "geglu", "mlp_up", "mlp", "linear", "moe"],
+                   choices=["gate_up", "down", "geglu", "mlp_up", "mlp", "mlp_decode", "linear",
+                            "moe"],
                    help="profiling aid: launch one entry point --launches times on random "
                         "inputs of --shape and exit (no timing, no JSON)")
     p.add_argument("--shape", default="8192,8192,8192", help="T,D,H for --profile-kernel")
@@ -764,9 +765,12 @@ def run_profile_case(args):
             fm.fmlp_geglu(x, W1, W2, W3, y, T, D, H, mid, mid.numel() * 2)
         elif k == "mlp_up":
             fm.fmlp_linear_bias_gelu(x, W1, b1, mid, T, D, H, fm.FMLP_GELU_ERF)
-        elif k == "mlp":
+        elif k in ("mlp", "mlp_decode"):
+            # mlp_decode: blocks of 1..4 tokens as the one-kernel decode (plan switch)
+            fm.fmlp_test_prefer_decode(1 if k == "mlp_decode" else 0)
             fm.fmlp_mlp_gelu(x, W1, b1, W3, b2, y, T, D, H, D, fm.FMLP_GELU_ERF, mid,
                              mid.numel() * 2)
+            fm.fmlp_test_prefer_decode(0)
         elif k == "linear":
             fm.fmlp_linear_bias(x, W1, b1, mid, T, D, H)
         elif k == "moe":

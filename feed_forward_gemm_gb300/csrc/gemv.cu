@@ -57,12 +57,14 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   return v;
 }
 
-// acc (even, odd element sums) += the 8 products of weight chunk w and x chunk (xa, xb).
-__device__ __forceinline__ void dot8x2(float2& acc, uint4 w, const float4& xa, const float4& xb) {
-  ffma2(acc, bf16_lo(w.x), bf16_hi(w.x), xa.x, xa.y);
-  ffma2(acc, bf16_lo(w.y), bf16_hi(w.y), xa.z, xa.w);
-  ffma2(acc, bf16_lo(w.z), bf16_hi(w.z), xb.x, xb.y);
-  ffma2(acc, bf16_lo(w.w), bf16_hi(w.w), xb.z, xb.w);
+// acc (packed even, odd element sums) += the 8 products of weight chunk w and the x chunk
+// given as four packed fp32 pairs.
+__device__ __forceinline__ void dot8p(uint64_t& acc, uint4 w, uint64_t x01, uint64_t x23,
+                                      uint64_t x45, uint64_t x67) {
+  ffma2p(acc, bf16x2_to_f2(w.x), x01);
+  ffma2p(acc, bf16x2_to_f2(w.y), x23);
+  ffma2p(acc, bf16x2_to_f2(w.z), x45);
+  ffma2p(acc, bf16x2_to_f2(w.w), x67);
 }
 
 // One layer for this CTA's rows [r0, r1) of W (NMAT matrices): y[t, n] for n in [r0, r1).
@@ -142,20 +144,24 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
   // accumulator pairs per token (two at one token, alternating between segments, so the
   // multiply-add chains are shorter; one at more tokens, where the tokens already interleave)
   constexpr int NA = TMAX == 1 ? 2 : 1;
-  float2 acc[TMAX][NA];
+  uint64_t acc[TMAX][NA];   // packed fp32 pairs; all-zero bits are (+0, +0)
 #pragma unroll
   for (int t = 0; t < TMAX; ++t)
 #pragma unroll
-    for (int k = 0; k < NA; ++k) acc[t][k] = make_float2(0.f, 0.f);
+    for (int k = 0; k < NA; ++k) acc[t][k] = 0ull;
   int piece_row = -1;   // (matrix, row) id of the run piece being accumulated
   auto flush = [&]() {
     float v[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
-      v[t] = acc[t][0].x + acc[t][0].y;
-      if (NA == 2) v[t] += acc[t][NA - 1].x + acc[t][NA - 1].y;
+      const float2 a0 = unpack_f2(acc[t][0]);
+      v[t] = a0.x + a0.y;
+      if (NA == 2) {
+        const float2 a1 = unpack_f2(acc[t][NA - 1]);
+        v[t] += a1.x + a1.y;
+      }
 #pragma unroll
-      for (int k = 0; k < NA; ++k) acc[t][k] = make_float2(0.f, 0.f);
+      for (int k = 0; k < NA; ++k) acc[t][k] = 0ull;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v[t] += __shfl_xor_sync(0xffffffffu, v[t], o);
     }
@@ -179,18 +185,20 @@ __device__ __forceinline__ void gemv_rows(uint8_t* gsm, const __nv_bfloat16* __r
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
-          float4 xa, xb;
+          uint64_t x01, x23, x45, x67;
           if (XF32) {
             const uint32_t xt = xs + static_cast<uint32_t>(t) * static_cast<uint32_t>(C) * 32u;
-            xa = lds_f4(xt + chunk * 16u);
-            xb = lds_f4(xt + static_cast<uint32_t>(C) * 16u + chunk * 16u);
+            lds_f2x2(xt + chunk * 16u, x01, x23);
+            lds_f2x2(xt + static_cast<uint32_t>(C) * 16u + chunk * 16u, x45, x67);
           } else {
             const uint4 xv = lds_v4(xs + (static_cast<uint32_t>(t) * static_cast<uint32_t>(C) +
                                           chunk) * 16u);
-            xa = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
-            xb = make_float4(bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w));
+            x01 = bf16x2_to_f2(xv.x);
+            x23 = bf16x2_to_f2(xv.y);
+            x45 = bf16x2_to_f2(xv.z);
+            x67 = bf16x2_to_f2(xv.w);
           }
-          dot8x2(acc[t][u % NA], wv[u], xa, xb);
+          dot8p(acc[t][u % NA], wv[u], x01, x23, x45, x67);
         }
       }
       // the register just used takes the load kGemvBatch segments ahead, so that the

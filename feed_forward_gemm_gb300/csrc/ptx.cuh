@@ -155,6 +155,36 @@ __device__ __forceinline__ void ffma2(float2& d, float ax, float ay, float bx, f
       : "f"(ax), "f"(ay), "f"(bx), "f"(by));
 }
 
+// Two fp32 values in one 64-bit register (low word first): the operand type of the packed
+// f32x2 instructions. Keeping accumulators and operands in this form avoids repacking at
+// every multiply-add.
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_f2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+// A bf16 pair (one 32-bit word, low element first) widened to a packed fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return pack_f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// d += a * b, lane-wise on packed fp32 pairs (each lane rounds like fmaf).
+__device__ __forceinline__ void ffma2p(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// Four fp32 from shared memory as two packed pairs.
+__device__ __forceinline__ void lds_f2x2(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+
 // ---------------------------------------------------------------- TMA (tensor copies)
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -357,6 +357,62 @@ fmlp_status check_alias(const Range& out, const Range* in, int n) {
 
 size_t mat_bytes(int64_t r, int64_t c) { return static_cast<size_t>(r) * static_cast<size_t>(c) * 2u; }
 
+// ------------------------------------------------------------------------- ragged dims
+// Inner dimensions that are not multiples of 8 run on zero-padded copies (pad.cu says why
+// that changes no result): the operands are copied into one stream-ordered scratch with every
+// inner dimension rounded up to 8, the normal plan runs on the padded shape, and the output's
+// first columns are copied back. Packed rows only (a strided call keeps the multiple-of-8
+// rule); it costs a copy of the weights per call.
+int64_t up8(int64_t v) { return (v + 7) / 8 * 8; }
+
+fmlp_status check_ragged(int64_t v, const char* name) {
+  if (v < 1 || v > kMaxDim - 7) {
+    set_error("%s = %lld must be in [1, 2^31-8]", name, static_cast<long long>(v));
+    return FMLP_ERR_SHAPE;
+  }
+  return FMLP_OK;
+}
+
+// Regions of one scratch allocation, each 256-byte aligned.
+struct PadScratch {
+  size_t sizes[8];
+  int n = 0;
+  void* base = nullptr;
+  size_t add(size_t bytes) {
+    sizes[n++] = (bytes + 255) / 256 * 256;
+    return static_cast<size_t>(n - 1);
+  }
+  size_t total() const {
+    size_t t = 0;
+    for (int i = 0; i < n; ++i) t += sizes[i];
+    return t;
+  }
+  void* at(size_t i) const {
+    size_t o = 0;
+    for (size_t k = 0; k < i; ++k) o += sizes[k];
+    return static_cast<char*>(base) + o;
+  }
+};
+
+fmlp_status pad_alloc(PadScratch* p, cudaStream_t st) {
+  cudaError_t e = cudaMallocAsync(&p->base, p->total(), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(padded operands)");
+  return FMLP_OK;
+}
+
+fmlp_status pad_free(PadScratch* p, cudaStream_t st, fmlp_status r) {
+  cudaError_t e = cudaFreeAsync(p->base, st);
+  if (e != cudaSuccess && r == FMLP_OK) return cuda_fail(e, "cudaFreeAsync(padded operands)");
+  return r;
+}
+
+fmlp_status pad_copy(const void* src, int64_t rows, int64_t cols, void* dst, int64_t dst_rows,
+                     int64_t dst_cols, cudaStream_t st) {
+  cudaError_t e = pad2d_launch(src, cols, rows, cols, dst, dst_rows, dst_cols, st);
+  if (e != cudaSuccess) return cuda_fail(e, "zero-padding copy");
+  return FMLP_OK;
+}
+
 // ------------------------------------------------------------------------- tile choice
 
 // Persistent grid: each CTA takes tiles round-robin, so the critical path is
@@ -792,24 +848,31 @@ const char* fmlp_last_error(void) { return t_last_error.c_str(); }
 
 // Every plan but the single-kernel small GeGLU keeps the intermediate (T x H bf16) in the
 // workspace, so the size depends on the shape alone.
+// With an inner dimension that is not a multiple of 8 the zero-padded path takes its own
+// scratch (intermediate included): no caller workspace.
 size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H) {
   if (T <= 0 || H <= 0) return 0;
+  if (D % 8 != 0 || H % 8 != 0) return 0;
   return plan_geglu(T, D, H, plan_sms()) == FMLP_PLAN_FUSED_SMALL ? 0 : mat_bytes(T, H);
 }
 
 size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout) {
   if (T <= 0 || H <= 0) return 0;
+  if (D % 8 != 0 || H % 8 != 0 || Dout % 8 != 0) return 0;
   return plan_mlp(T, D, H, Dout, plan_sms()) == FMLP_PLAN_FUSED_SMALL ? 0 : mat_bytes(T, H);
 }
 
-int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) { return plan_geglu(T, D, H, plan_sms()); }
+// Plans of ragged sizes are those of the zero-padded shape.
+int fmlp_geglu_plan(int64_t T, int64_t D, int64_t H) {
+  return plan_geglu(T, up8(D), up8(H), plan_sms());
+}
 
 int fmlp_mlp_gelu_plan(int64_t T, int64_t D, int64_t H, int64_t Dout) {
-  return plan_mlp(T, D, H, Dout, plan_sms());
+  return plan_mlp(T, up8(D), up8(H), up8(Dout), plan_sms());
 }
 
 int fmlp_linear_plan(int64_t T, int64_t in, int64_t out) {
-  return plan_linear(T, in, out, plan_sms());
+  return plan_linear(T, up8(in), up8(out), plan_sms());
 }
 
 // Row strides of x [T, in] and y [T, out] in elements: 0 means packed rows (the stride is
@@ -835,9 +898,54 @@ static fmlp_status resolve_strides(int64_t* ldx, int64_t* ldy, int64_t in, int64
 // ldx, ldy: row strides of x and y in elements (0: packed rows).
 static fmlp_status linear_common(const void* x, const void* W, const void* b, void* y,
                                  int64_t T, int64_t in, int64_t out, int epi, int mode,
-                                 fmlp_stream_t s, int64_t ldx = 0, int64_t ldy = 0) {
+                                 fmlp_stream_t s, int64_t ldx = 0, int64_t ldy = 0);
+
+// A Linear (or Linear + activation) whose in or out is not a multiple of 8.
+static fmlp_status linear_padded(const void* x, const void* W, const void* b, void* y,
+                                 int64_t T, int64_t in, int64_t out, int epi, int mode,
+                                 fmlp_stream_t s) {
+  FMLP_TRY(check_ragged(in, "in"));
+  FMLP_TRY(check_ragged(out, "out"));
+  if (epi == EPI_BIAS_GELU && !act_mode_ok(mode)) {
+    set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU", mode);
+    return FMLP_ERR_SHAPE;
+  }
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(W, "W");
+  FMLP_NONNULL(y, "y");
+  const Range rx{x, mat_bytes(T, in), "x"}, rw{W, mat_bytes(out, in), "W"},
+      rb{b, b ? mat_bytes(1, out) : 0, "b"}, ry{y, mat_bytes(T, out), "y"};
+  const Range ins[3] = {rx, rw, rb};
+  const Range all[4] = {rx, rw, rb, ry};
+  FMLP_TRY(check_ptrs(all, 4));
+  FMLP_TRY(check_alias(ry, ins, 3));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int64_t Kp = up8(in), Np = up8(out);
+  PadScratch p;
+  const size_t ix = p.add(mat_bytes(T, Kp)), iw = p.add(mat_bytes(Np, Kp)),
+               ib = p.add(b ? mat_bytes(1, Np) : 0), iy = p.add(mat_bytes(T, Np));
+  FMLP_TRY(pad_alloc(&p, st));
+  fmlp_status r = pad_copy(x, T, in, p.at(ix), T, Kp, st);
+  if (r == FMLP_OK) r = pad_copy(W, out, in, p.at(iw), Np, Kp, st);
+  if (r == FMLP_OK && b) r = pad_copy(b, 1, out, p.at(ib), 1, Np, st);
+  if (r == FMLP_OK)
+    r = linear_common(p.at(ix), p.at(iw), b ? p.at(ib) : nullptr, p.at(iy), T, Kp, Np, epi,
+                      mode, s);
+  if (r == FMLP_OK) {
+    cudaError_t e = copy2d_launch(p.at(iy), Np, y, out, T, out, st);
+    if (e != cudaSuccess) r = cuda_fail(e, "unpadding copy");
+  }
+  return pad_free(&p, st, r);
+}
+
+static fmlp_status linear_common(const void* x, const void* W, const void* b, void* y,
+                                 int64_t T, int64_t in, int64_t out, int epi, int mode,
+                                 fmlp_stream_t s, int64_t ldx, int64_t ldy) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
+  if ((in % 8 != 0 || out % 8 != 0) && ldx == 0 && ldy == 0)
+    return linear_padded(x, W, b, y, T, in, out, epi, mode, s);
   FMLP_TRY(check_inner(in, "in"));
   FMLP_TRY(check_inner(out, "out"));
   FMLP_TRY(resolve_strides(&ldx, &ldy, in, out));
@@ -885,6 +993,37 @@ fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, vo
                                int64_t D, int64_t H, fmlp_stream_t s) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
+  if (D % 8 != 0 || H % 8 != 0) {
+    // zero-padded copies of x, Wg, Wu; m's first H columns copied back
+    FMLP_TRY(check_ragged(D, "D"));
+    FMLP_TRY(check_ragged(H, "H"));
+    if (T == 0) return FMLP_OK;
+    FMLP_NONNULL(x, "x");
+    FMLP_NONNULL(Wg, "Wg");
+    FMLP_NONNULL(Wu, "Wu");
+    FMLP_NONNULL(m, "m");
+    const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, mat_bytes(H, D), "Wg"},
+        ru{Wu, mat_bytes(H, D), "Wu"}, rm{m, mat_bytes(T, H), "m"};
+    const Range ins[3] = {rx, rg, ru};
+    const Range all[4] = {rx, rg, ru, rm};
+    FMLP_TRY(check_ptrs(all, 4));
+    FMLP_TRY(check_alias(rm, ins, 3));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+    const int64_t Dp = up8(D), Hp = up8(H);
+    PadScratch p;
+    const size_t ix = p.add(mat_bytes(T, Dp)), ig = p.add(mat_bytes(Hp, Dp)),
+                 iu = p.add(mat_bytes(Hp, Dp)), im = p.add(mat_bytes(T, Hp));
+    FMLP_TRY(pad_alloc(&p, st));
+    fmlp_status r = pad_copy(x, T, D, p.at(ix), T, Dp, st);
+    if (r == FMLP_OK) r = pad_copy(Wg, H, D, p.at(ig), Hp, Dp, st);
+    if (r == FMLP_OK) r = pad_copy(Wu, H, D, p.at(iu), Hp, Dp, st);
+    if (r == FMLP_OK) r = fmlp_geglu_gate_up(p.at(ix), p.at(ig), p.at(iu), p.at(im), T, Dp, Hp, s);
+    if (r == FMLP_OK) {
+      cudaError_t e = copy2d_launch(p.at(im), Hp, m, H, T, H, st);
+      if (e != cudaSuccess) r = cuda_fail(e, "unpadding copy");
+    }
+    return pad_free(&p, st, r);
+  }
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
   if (T == 0) return FMLP_OK;
@@ -909,9 +1048,53 @@ fmlp_status fmlp_geglu_gate_up(const void* x, const void* Wg, const void* Wu, vo
 // ldx, ldy: row strides of x and y in elements (0: packed rows).
 static fmlp_status geglu_common(const void* x, int64_t ldx, const void* Wg, const void* Wu,
                                 const void* Wd, void* y, int64_t ldy, int64_t T, int64_t D,
+                                int64_t H, void* ws, size_t ws_bytes, fmlp_stream_t s);
+
+// The GeGLU block with D or H not a multiple of 8 (the caller's workspace is not used).
+static fmlp_status geglu_padded(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                                void* y, int64_t T, int64_t D, int64_t H, fmlp_stream_t s) {
+  FMLP_TRY(check_ragged(D, "D"));
+  FMLP_TRY(check_ragged(H, "H"));
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(Wg, "Wg");
+  FMLP_NONNULL(Wu, "Wu");
+  FMLP_NONNULL(Wd, "Wd");
+  FMLP_NONNULL(y, "y");
+  const Range rx{x, mat_bytes(T, D), "x"}, rg{Wg, mat_bytes(H, D), "Wg"},
+      ru{Wu, mat_bytes(H, D), "Wu"}, rd{Wd, mat_bytes(D, H), "Wd"}, ry{y, mat_bytes(T, D), "y"};
+  const Range ins[4] = {rx, rg, ru, rd};
+  const Range all[5] = {rx, rg, ru, rd, ry};
+  FMLP_TRY(check_ptrs(all, 5));
+  FMLP_TRY(check_alias(ry, ins, 4));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int64_t Dp = up8(D), Hp = up8(H);
+  PadScratch p;
+  const size_t ix = p.add(mat_bytes(T, Dp)), ig = p.add(mat_bytes(Hp, Dp)),
+               iu = p.add(mat_bytes(Hp, Dp)), id = p.add(mat_bytes(Dp, Hp)),
+               iy = p.add(mat_bytes(T, Dp));
+  FMLP_TRY(pad_alloc(&p, st));
+  fmlp_status r = pad_copy(x, T, D, p.at(ix), T, Dp, st);
+  if (r == FMLP_OK) r = pad_copy(Wg, H, D, p.at(ig), Hp, Dp, st);
+  if (r == FMLP_OK) r = pad_copy(Wu, H, D, p.at(iu), Hp, Dp, st);
+  if (r == FMLP_OK) r = pad_copy(Wd, D, H, p.at(id), Dp, Hp, st);
+  if (r == FMLP_OK)
+    r = geglu_common(p.at(ix), 0, p.at(ig), p.at(iu), p.at(id), p.at(iy), 0, T, Dp, Hp, nullptr,
+                     0, s);
+  if (r == FMLP_OK) {
+    cudaError_t e = copy2d_launch(p.at(iy), Dp, y, D, T, D, st);
+    if (e != cudaSuccess) r = cuda_fail(e, "unpadding copy");
+  }
+  return pad_free(&p, st, r);
+}
+
+static fmlp_status geglu_common(const void* x, int64_t ldx, const void* Wg, const void* Wu,
+                                const void* Wd, void* y, int64_t ldy, int64_t T, int64_t D,
                                 int64_t H, void* ws, size_t ws_bytes, fmlp_stream_t s) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
+  if ((D % 8 != 0 || H % 8 != 0) && ldx == 0 && ldy == 0)
+    return geglu_padded(x, Wg, Wu, Wd, y, T, D, H, s);
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
   FMLP_TRY(resolve_strides(&ldx, &ldy, D, D));
@@ -1087,9 +1270,62 @@ fmlp_status fmlp_moe_geglu(const void* x, const int32_t* offsets, int64_t E, con
 static fmlp_status mlp_common(const void* x, int64_t ldx, const void* W1, const void* b1,
                               const void* W2, const void* b2, void* y, int64_t ldy, int64_t T,
                               int64_t D, int64_t H, int64_t Dout, fmlp_gelu_mode mode, void* ws,
+                              size_t ws_bytes, fmlp_stream_t s);
+
+// The MLP block with D, H or Dout not a multiple of 8 (the caller's workspace is not used).
+static fmlp_status mlp_padded(const void* x, const void* W1, const void* b1, const void* W2,
+                              const void* b2, void* y, int64_t T, int64_t D, int64_t H,
+                              int64_t Dout, fmlp_gelu_mode mode, fmlp_stream_t s) {
+  FMLP_TRY(check_ragged(D, "D"));
+  FMLP_TRY(check_ragged(H, "H"));
+  FMLP_TRY(check_ragged(Dout, "Dout"));
+  if (!act_mode_ok(mode)) {
+    set_error("activation mode %d is not FMLP_GELU_TANH, FMLP_GELU_ERF or FMLP_RELU",
+              static_cast<int>(mode));
+    return FMLP_ERR_SHAPE;
+  }
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(W1, "W1");
+  FMLP_NONNULL(W2, "W2");
+  FMLP_NONNULL(y, "y");
+  const Range rx{x, mat_bytes(T, D), "x"}, r1{W1, mat_bytes(H, D), "W1"},
+      rb1{b1, b1 ? mat_bytes(1, H) : 0, "b1"}, r2{W2, mat_bytes(Dout, H), "W2"},
+      rb2{b2, b2 ? mat_bytes(1, Dout) : 0, "b2"}, ry{y, mat_bytes(T, Dout), "y"};
+  const Range ins[5] = {rx, r1, rb1, r2, rb2};
+  const Range all[6] = {rx, r1, rb1, r2, rb2, ry};
+  FMLP_TRY(check_ptrs(all, 6));
+  FMLP_TRY(check_alias(ry, ins, 5));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int64_t Dp = up8(D), Hp = up8(H), Op = up8(Dout);
+  PadScratch p;
+  const size_t ix = p.add(mat_bytes(T, Dp)), i1 = p.add(mat_bytes(Hp, Dp)),
+               ib1 = p.add(b1 ? mat_bytes(1, Hp) : 0), i2 = p.add(mat_bytes(Op, Hp)),
+               ib2 = p.add(b2 ? mat_bytes(1, Op) : 0), iy = p.add(mat_bytes(T, Op));
+  FMLP_TRY(pad_alloc(&p, st));
+  fmlp_status r = pad_copy(x, T, D, p.at(ix), T, Dp, st);
+  if (r == FMLP_OK) r = pad_copy(W1, H, D, p.at(i1), Hp, Dp, st);
+  if (r == FMLP_OK && b1) r = pad_copy(b1, 1, H, p.at(ib1), 1, Hp, st);
+  if (r == FMLP_OK) r = pad_copy(W2, Dout, H, p.at(i2), Op, Hp, st);
+  if (r == FMLP_OK && b2) r = pad_copy(b2, 1, Dout, p.at(ib2), 1, Op, st);
+  if (r == FMLP_OK)
+    r = mlp_common(p.at(ix), 0, p.at(i1), b1 ? p.at(ib1) : nullptr, p.at(i2),
+                   b2 ? p.at(ib2) : nullptr, p.at(iy), 0, T, Dp, Hp, Op, mode, nullptr, 0, s);
+  if (r == FMLP_OK) {
+    cudaError_t e = copy2d_launch(p.at(iy), Op, y, Dout, T, Dout, st);
+    if (e != cudaSuccess) r = cuda_fail(e, "unpadding copy");
+  }
+  return pad_free(&p, st, r);
+}
+
+static fmlp_status mlp_common(const void* x, int64_t ldx, const void* W1, const void* b1,
+                              const void* W2, const void* b2, void* y, int64_t ldy, int64_t T,
+                              int64_t D, int64_t H, int64_t Dout, fmlp_gelu_mode mode, void* ws,
                               size_t ws_bytes, fmlp_stream_t s) {
   t_last_error.clear();
   FMLP_TRY(check_T(T));
+  if ((D % 8 != 0 || H % 8 != 0 || Dout % 8 != 0) && ldx == 0 && ldy == 0)
+    return mlp_padded(x, W1, b1, W2, b2, y, T, D, H, Dout, mode, s);
   FMLP_TRY(check_inner(D, "D"));
   FMLP_TRY(check_inner(H, "H"));
   FMLP_TRY(check_inner(Dout, "Dout"));
@@ -1232,29 +1468,39 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
   DeviceState* d = nullptr;
   FMLP_TRY(device_state(&d));
   std::string r;
+  if (T > 0 && (D % 8 != 0 || H % 8 != 0 || (op == 4 && Dout % 8 != 0))) {
+    char b[200];
+    snprintf(b, sizeof b, "zero-padded copies (inner dims %lld, %lld%s%s -> multiples of 8), then ",
+             static_cast<long long>(D), static_cast<long long>(H), op == 4 ? ", " : "",
+             op == 4 ? std::to_string(static_cast<long long>(Dout)).c_str() : "");
+    r = b;
+    D = up8(D);
+    H = up8(H);
+    Dout = up8(Dout);
+  }
   if (T <= 0) {
     r = "nothing launched (T = 0)";
   } else if (op == 0 || op == 1) {   // linear (+gelu): D -> H
     const int epi = op == 0 ? EPI_BIAS : EPI_BIAS_GELU;
-    r = plan_linear(T, D, H, d->sms) == FMLP_PLAN_GEMV ? describe_gemv(*d, "linear", T, D, H)
-                                                       : describe_gemm(*d, "linear", epi, T, H, D);
+    r += plan_linear(T, D, H, d->sms) == FMLP_PLAN_GEMV ? describe_gemv(*d, "linear", T, D, H)
+                                                        : describe_gemm(*d, "linear", epi, T, H, D);
   } else if (op == 2) {              // gate/up
-    r = gemv_ok(T, D, H, 2, d->sms) && gemv_preferred(T, 2 * mat_bytes(H, D))
-            ? describe_gemv(*d, "gate/up", T, D, H, 2)
-                                    : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
+    r += gemv_ok(T, D, H, 2, d->sms) && gemv_preferred(T, 2 * mat_bytes(H, D))
+             ? describe_gemv(*d, "gate/up", T, D, H, 2)
+             : describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D);
   } else if (op == 3) {              // geglu block
     const int p = plan_geglu(T, D, H, d->sms);
     if (p == FMLP_PLAN_DECODE) {
-      r = describe_decode(*d, "GeGLU block", T, D, H, D, 2);
+      r += describe_decode(*d, "GeGLU block", T, D, H, D, 2);
     } else if (p == FMLP_PLAN_FUSED_SMALL) {
       char b[160];
       snprintf(b, sizeof b, "fused block: one kernel, grid=%lld", static_cast<long long>((T + 127) / 128));
-      r = b;
+      r += b;
     } else if (p == FMLP_PLAN_GEMV) {
-      r = describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
+      r += describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
     } else {
-      r = describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
-          describe_gemm(*d, "down", EPI_BIAS, T, D, H);
+      r += describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
+           describe_gemm(*d, "down", EPI_BIAS, T, D, H);
     }
   } else if (op == 4) {              // mlp: D -> H -> Dout
     const int p = plan_mlp(T, D, H, Dout, d->sms);
@@ -1262,14 +1508,14 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       char b[160];
       snprintf(b, sizeof b, "fused block: one kernel, grid=%lld",
                static_cast<long long>((T + 127) / 128));
-      r = b;
+      r += b;
     } else if (p == FMLP_PLAN_DECODE)
-      r = describe_decode(*d, "MLP block", T, D, H, Dout, 1);
+      r += describe_decode(*d, "MLP block", T, D, H, Dout, 1);
     else if (p == FMLP_PLAN_GEMV)
-      r = describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
+      r += describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
     else
-      r = describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
-          describe_gemm(*d, "down", EPI_BIAS, T, Dout, H);
+      r += describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
+           describe_gemm(*d, "down", EPI_BIAS, T, Dout, H);
   } else {
     set_error("op %d unknown", op);
     return FMLP_ERR_SHAPE;

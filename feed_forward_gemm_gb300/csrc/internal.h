@@ -88,6 +88,14 @@ struct SkinnyLaunch {
   uint64_t timeout_ns;
 };
 cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
+
+// Zero-padded copies (pad.cu): dst [dst_rows, dst_cols] (dst_cols a multiple of 8) takes
+// src [rows, cols] (row stride ld) and zeros elsewhere; copy2d copies rows x cols between
+// row strides.
+cudaError_t pad2d_launch(const void* src, int64_t ld, int64_t rows, int64_t cols, void* dst,
+                         int64_t dst_rows, int64_t dst_cols, cudaStream_t s);
+cudaError_t copy2d_launch(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, cudaStream_t s);
 // Clusters of `split` few-token CTAs that can be resident at once (the GPCs decide how many
 // clusters of a size fit, not just the SM count).
 cudaError_t gemm_skinny_max_clusters(int split, int* clusters);

@@ -45,8 +45,10 @@
  *     (cudaDeviceReset) while the library is loaded leaves them stale and is not supported.
  *   - Requirements checked before anything is launched (the status names the first failure):
  *       FMLP_ERR_NULL       a required pointer is NULL
- *       FMLP_ERR_SHAPE      T < 0, or an inner dimension (in/out/D/H/Dout) < 1 or not a
- *                           multiple of 8, or a dimension above 2^31 - 1
+ *       FMLP_ERR_SHAPE      T < 0, or an inner dimension (in/out/D/H/Dout) < 1, or a
+ *                           dimension above 2^31 - 8; for the strided calls (with a row
+ *                           stride given), fmlp_moe_geglu and fmlp_geglu_noalloc also an
+ *                           inner dimension that is not a multiple of 8
  *       FMLP_ERR_ALIGN      a tensor pointer not 16-byte aligned
  *       FMLP_ERR_ALIAS      the output overlaps an input (or the workspace)
  *       FMLP_ERR_WORKSPACE  ws_bytes smaller than the matching *_workspace_size()
@@ -227,8 +229,19 @@ FMLP_API fmlp_status fmlp_geglu_noalloc(const void* x, const void* Wg, const voi
                                         const void* Wd, void* y, int64_t T, int64_t D, int64_t H,
                                         fmlp_stream_t s);
 
-/* Workspace bytes the calls above need (T*H*2 for the 2-kernel plans, else 0). Pure host
- * functions; they touch no device. */
+/* Inner dimensions that are not multiples of 8 (packed rows). The TMA loads and stores move
+ * rows whose byte stride is a multiple of 16, so such a call copies its operands, zero-padded
+ * to the next multiple of 8 in every inner dimension, into one scratch taken from the
+ * stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on the call's stream), runs the plan
+ * of the padded shape, and copies the output's columns back: exact (zero columns add nothing,
+ * padded outputs are dropped, a zero gate/up or first-layer row gives gelu(0) or act(0) = 0),
+ * at the cost of one extra read and write of every operand. The caller's workspace is not
+ * used (the workspace queries return 0 for such sizes); the plan queries report the padded
+ * shape's plan. "Profiling in PyTorch (Part 2)", section "What's the transpose doing?": the
+ * copy changes only the strides the kernels see. */
+
+/* Workspace bytes the calls above need (T*H*2 for the 2-kernel plans, else 0; 0 for inner
+ * dimensions that are not multiples of 8). Pure host functions; they touch no device. */
 FMLP_API size_t fmlp_geglu_workspace_size(int64_t T, int64_t D, int64_t H);
 FMLP_API size_t fmlp_mlp_gelu_workspace_size(int64_t T, int64_t D, int64_t H, int64_t Dout);
 

@@ -63,6 +63,17 @@ def test_workspace_sizes_and_counts(lib):
     assert fm.fmlp_geglu_workspace_size(0, 768, 3072) == 0
 
 
+def test_ragged_sizes_plan_as_their_padded_shape(lib):
+    """Inner dims that are not multiples of 8 take the plan of the zero-padded shape and need
+    no workspace from the caller (the padded path takes its own scratch)."""
+    assert fm.fmlp_geglu_plan(8192, 766, 3070) == fm.fmlp_geglu_plan(8192, 768, 3072)
+    assert fm.fmlp_mlp_gelu_plan(1, 4093, 4096, 4090) == fm.fmlp_mlp_gelu_plan(1, 4096, 4096, 4096)
+    assert fm.fmlp_linear_plan(3, 100, 37) == fm.fmlp_linear_plan(3, 104, 40)
+    assert fm.fmlp_geglu_workspace_size(8192, 766, 3072) == 0
+    assert fm.fmlp_mlp_gelu_workspace_size(16, 64, 64, 60) == 0
+    assert fm.fmlp_geglu_workspace_size(8192, 768, 3072) == 8192 * 3072 * 2
+
+
 def test_plans_are_pure_host(lib):
     assert fm.fmlp_geglu_plan(0, 768, 3072) == fm.FMLP_PLAN_NONE
     assert fm.fmlp_geglu_plan(8192, 768, 3072) == fm.FMLP_PLAN_TC
@@ -80,7 +91,15 @@ def test_linear_validation(lib):
     assert call_linear(y=0) == fm.FMLP_ERR_NULL
     assert call_linear(T=-1) == fm.FMLP_ERR_SHAPE
     assert call_linear(i=0) == fm.FMLP_ERR_SHAPE
-    assert call_linear(i=12) == fm.FMLP_ERR_SHAPE          # not a multiple of 8
+    # in or out not a multiple of 8: the zero-padded path, with the same checks first
+    assert call_linear(i=12, T=0) == fm.FMLP_OK
+    assert call_linear(i=12, x=0) == fm.FMLP_ERR_NULL
+    assert call_linear(i=12, x=A + 8) == fm.FMLP_ERR_ALIGN
+    assert call_linear(o=20, y=A + 16) == fm.FMLP_ERR_ALIAS
+    assert call_linear(i=2**31 - 5) == fm.FMLP_ERR_SHAPE
+    # ... but a strided call keeps the multiple-of-8 rule
+    assert fm.fmlp_linear_bias_strided(A, A + GB, None, A + 3 * GB, 16, 12, 64, ldx=16, ldy=64,
+                                       stream=0, raise_on_error=False) == fm.FMLP_ERR_SHAPE
     assert call_linear(o=2**31) == fm.FMLP_ERR_SHAPE
     assert call_linear(x=A + 8) == fm.FMLP_ERR_ALIGN
     assert call_linear(b=A + 2 * GB + 2) == fm.FMLP_ERR_ALIGN
@@ -99,7 +118,11 @@ def test_geglu_validation(lib):
         return fm.fmlp_geglu(a["x"], a["Wg"], a["Wu"], a["Wd"], a["y"], a["T"], a["D"], a["H"],
                              a["ws"], a["ws_bytes"], stream=0, raise_on_error=False)
     assert call(Wu=0) == fm.FMLP_ERR_NULL
-    assert call(H=100) == fm.FMLP_ERR_SHAPE
+    assert call(H=100, T=0) == fm.FMLP_OK                  # zero-padded path
+    assert call(H=100, Wu=0) == fm.FMLP_ERR_NULL
+    assert fm.fmlp_geglu_strided(A, A + GB, A + 2 * GB, A + 3 * GB, A + 4 * GB, 128, 512, 100,
+                                 A + 5 * GB, 1 << 20, ldx=520, ldy=520, stream=0,
+                                 raise_on_error=False) == fm.FMLP_ERR_SHAPE
     assert call(ws_bytes=100) == fm.FMLP_ERR_WORKSPACE
     assert call(ws=A + 4 * GB) == fm.FMLP_ERR_ALIAS         # workspace on top of y
     assert call(ws=A + 3 * GB) == fm.FMLP_ERR_ALIAS         # workspace on top of Wd
@@ -120,7 +143,9 @@ def test_mlp_validation(lib):
     assert call(mode=7) == fm.FMLP_ERR_SHAPE
     assert call(mode=3, T=0) == fm.FMLP_ERR_SHAPE          # checked before the T == 0 exit
     assert call(mode=fm.FMLP_RELU, T=0) == fm.FMLP_OK
-    assert call(Do=6) == fm.FMLP_ERR_SHAPE
+    assert call(Do=6, T=0) == fm.FMLP_OK                   # zero-padded path
+    assert call(Do=6, mode=7) == fm.FMLP_ERR_SHAPE
+    assert call(Do=6, W2=0) == fm.FMLP_ERR_NULL
     assert call(y=A + 4 * GB) == fm.FMLP_ERR_ALIAS          # y on top of b2
     assert call(T=0) == fm.FMLP_OK
 

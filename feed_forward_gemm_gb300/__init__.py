@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "FmlpError", "load", "build", "library_path",
-    "fmlp_linear_bias", "fmlp_linear_bias_strided", "fmlp_linear_bias_gelu",
+    "fmlp_linear_bias", "fmlp_linear_bias_strided", "fmlp_linear_bias_gelu", "fmlp_linear_bias_wt",
     "fmlp_geglu_strided", "fmlp_mlp_gelu_strided",
     "fmlp_geglu_gate_up", "fmlp_geglu", "fmlp_moe_geglu", "fmlp_moe_geglu_workspace_size",
     "fmlp_mlp_gelu", "fmlp_geglu_workspace_size", "fmlp_mlp_gelu_workspace_size",
@@ -52,6 +52,7 @@ _INT = ctypes.c_int
 # name -> (restype, argtypes); the order matches include/fmlp.h
 _SIGNATURES = {
     "fmlp_linear_bias": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fmlp_linear_bias_wt": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fmlp_linear_bias_strided": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "fmlp_moe_geglu": (_INT, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_size_t,
                               _P]),
@@ -171,6 +172,13 @@ def fmlp_linear_bias(x, W, b, y, T, in_dim, out_dim, stream=None, raise_on_error
     st = load().fmlp_linear_bias(_ptr(x), _ptr(W), _ptr(b), _ptr(y), T, in_dim, out_dim,
                                  _stream(stream))
     return _check(st, "fmlp_linear_bias", raise_on_error)
+
+
+def fmlp_linear_bias_wt(x, Wt, b, y, T, in_dim, out_dim, stream=None, raise_on_error=True):
+    """y = x @ Wt + b with the weight given as [in, out] (the transposed layout)."""
+    st = load().fmlp_linear_bias_wt(_ptr(x), _ptr(Wt), _ptr(b), _ptr(y), T, in_dim, out_dim,
+                                    _stream(stream))
+    return _check(st, "fmlp_linear_bias_wt", raise_on_error)
 
 
 def _view(t, ld):

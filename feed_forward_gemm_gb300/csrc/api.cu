@@ -983,6 +983,48 @@ fmlp_status fmlp_linear_bias_strided(const void* x, int64_t ldx, const void* W, 
   return linear_common(x, W, b, y, T, in, out, EPI_BIAS, 0, s, ldx, ldy);
 }
 
+fmlp_status fmlp_linear_bias_wt(const void* x, const void* Wt, const void* b, void* y,
+                                int64_t T, int64_t in, int64_t out, fmlp_stream_t s) {
+  t_last_error.clear();
+  FMLP_TRY(check_T(T));
+  FMLP_TRY(check_inner(in, "in"));
+  FMLP_TRY(check_inner(out, "out"));
+  if (T == 0) return FMLP_OK;
+  FMLP_NONNULL(x, "x");
+  FMLP_NONNULL(Wt, "Wt");
+  FMLP_NONNULL(y, "y");
+  const Range rx{x, mat_bytes(T, in), "x"}, rw{Wt, mat_bytes(in, out), "Wt"},
+      rb{b, b ? mat_bytes(1, out) : 0, "b"}, ry{y, mat_bytes(T, out), "y"};
+  const Range ins[3] = {rx, rw, rb};
+  const Range all[4] = {rx, rw, rb, ry};
+  FMLP_TRY(check_ptrs(all, 4));
+  FMLP_TRY(check_alias(ry, ins, 3));
+  DeviceState* d = nullptr;
+  FMLP_TRY(device_state(&d));
+  FMLP_LAUNCH_GUARD("gemm_tc (transposed weights) launch");
+  GemmLaunch L;
+  memset(&L, 0, sizeof L);
+  double cost = 0;
+  L.bn = pick_bn(T, out, d->sms, false, &cost) >= 256 ? 256 : 128;
+  FMLP_TRY(make_map(&L.tmA, x, T, in, 128, "x"));
+  FMLP_TRY(make_map(&L.tmB0, Wt, in, out, 64, "Wt"));   // [in, out]: boxes of 64 out x 64 in
+  L.tmB1 = L.tmB0;
+  FMLP_TRY(make_map(&L.tmY, y, T, out, 32, "y"));
+  L.bias = b;
+  L.M = static_cast<int>(T);
+  L.N_out = static_cast<int>(out);
+  L.K = static_cast<int>(in);
+  L.epi = EPI_BIAS;
+  L.stream = reinterpret_cast<cudaStream_t>(s);
+  L.status = d->status;
+  L.timeout_ns = kWaitTimeoutNs;
+  const int64_t tiles = ((T + 127) / 128) * ((out + L.bn - 1) / L.bn);
+  L.grid = static_cast<int>(std::min<int64_t>(tiles, d->sms));
+  const cudaError_t e = gemm_tc_wt_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_tc (transposed weights) launch");
+  return FMLP_OK;
+}
+
 fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,
                                   int64_t T, int64_t in, int64_t out, fmlp_gelu_mode mode,
                                   fmlp_stream_t s) {

@@ -90,7 +90,12 @@ __device__ __forceinline__ void group_tile(int t, const int* s_off, const int* s
   rows = min(kBM, s_off[e + 1] - row0);
 }
 
-template <int BN, int EPI, bool GROUPED>
+// B_MN: the weights come as Wt [K, N_out] (N contiguous, the transposed `nn` layout), loaded
+// as BN / 64 boxes of 64 N columns x 64 K rows and read by the MMA as an MN-major operand;
+// no transposed copy is made ("Profiling in PyTorch (Part 2)", section "Where did the
+// transpose go? Kernel layouts and pre-ops": the layout is the kernel's choice of operand
+// major-ness).
+template <int BN, int EPI, bool GROUPED, bool B_MN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
@@ -199,6 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               tma_load_3d(sB, &tmB0, &full[stage], kb * kBK, tn * BN, ge);
             }
+          } else if (B_MN) {
+            // Wt [K, N]: box j holds N columns [tn BN + 64 j, + 64) of K rows [kb 64, + 64)
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sB + j * (64 * kBK * 2), &tmB0, &full[stage], tn * BN + 64 * j,
+                          kb * kBK);
           } else if (EPI == EPI_GEGLU) {
             tma_load_2d(sB, &tmB0, &full[stage], kb * kBK, tn * (BN / 2));
             tma_load_2d(sB + (BN / 2) * 128, &tmB1, &full[stage], kb * kBK, tn * (BN / 2));
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      constexpr uint32_t idesc = B_MN ? idesc_bf16_f32_bmn(kBM, BN) : idesc_bf16_f32(kBM, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -241,11 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stages + stage * C::STAGE_BYTES);
           const uint64_t a_desc = sdesc_kmajor_sw128(a_addr);
-          const uint64_t b_desc = sdesc_kmajor_sw128(a_addr + C::A_BYTES);
+          const uint64_t b_desc = B_MN ? sdesc_mnmajor_sw128(a_addr + C::A_BYTES, 64 * kBK * 2)
+                                       : sdesc_kmajor_sw128(a_addr + C::A_BYTES);
+          // advancing K by 16: 32 bytes along a K-major 128-byte row, or 16 rows (2048 bytes)
+          // of an MN-major tile
+          constexpr uint64_t b_step = B_MN ? (2048u >> 4) : 2u;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // advance 16 elements (32 bytes) along K inside the 128-byte swizzle row
-            tc_mma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+            tc_mma_bf16(d_tmem, a_desc + 2u * kk, b_desc + b_step * kk, idesc,
                         (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -311,10 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------- host side
 
-template <int BN, int EPI, bool GROUPED = false>
+template <int BN, int EPI, bool GROUPED = false, bool B_MN = false>
 static cudaError_t launch_one(const GemmLaunch& L) {
   using C = Cfg<BN, EPI>;
-  auto kern = gemm_tc_kernel<BN, EPI, GROUPED>;
+  auto kern = gemm_tc_kernel<BN, EPI, GROUPED, B_MN>;
   static SmemAttrCache cache;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, cache);
   if (e != cudaSuccess) return e;
@@ -344,6 +358,14 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L) {
     case EPI_BIAS_GELU * 1000 + 256: return launch_one<256, EPI_BIAS_GELU>(L);
     case EPI_GEGLU * 1000 + 128: return launch_one<128, EPI_GEGLU>(L);
     case EPI_GEGLU * 1000 + 256: return launch_one<256, EPI_GEGLU>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t gemm_tc_wt_launch(const GemmLaunch& L) {
+  switch (L.epi * 1000 + L.bn) {
+    case EPI_BIAS * 1000 + 128: return launch_one<128, EPI_BIAS, false, true>(L);
+    case EPI_BIAS * 1000 + 256: return launch_one<256, EPI_BIAS, false, true>(L);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -101,6 +101,9 @@ cudaError_t copy2d_launch(const void* src, int64_t ld_src, void* dst, int64_t ld
 cudaError_t gemm_skinny_max_clusters(int split, int* clusters);
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L);
+// The single-SM kernel with the weights given as Wt [K, N_out] (N contiguous; tmB0 a map of
+// Wt with a {64, 64} box), read as an MN-major operand; EPI_BIAS, bn 128 or 256.
+cudaError_t gemm_tc_wt_launch(const GemmLaunch& L);
 // The single-SM kernel over expert groups (bn 256; EPI_GEGLU or EPI_BIAS).
 cudaError_t gemm_tc_grouped_launch(const GemmLaunch& L);
 // CTA-pair (cta_group::2) kernel: 256 x 256 tiles over clusters of two CTAs; bn is 256;

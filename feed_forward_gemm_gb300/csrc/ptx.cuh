@@ -450,10 +450,31 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile in the 128-byte-swizzle layout: rows
+// of 128 bytes hold 64 consecutive M/N elements of one K index (a TMA box of 64 elements by K
+// rows, loaded from a [K, N] matrix whose N is contiguous); 8-row K groups are 1024 bytes
+// apart (stride byte offset) and 64-element M/N chunks `mn_chunk_bytes` apart (leading byte
+// offset). Advancing K by 16 moves the start address by 16 rows = 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr,
+                                                        uint32_t mn_chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_chunk_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16
 // (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with B MN-major (bit 16): B given as a [K, N] tile, N contiguous.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 }  // namespace fmlp

@@ -129,6 +129,16 @@ FMLP_API fmlp_status fmlp_linear_bias_strided(const void* x, int64_t ldx, const 
                                               const void* b, void* y, int64_t ldy, int64_t T,
                                               int64_t in, int64_t out, fmlp_stream_t s);
 
+/* y[T, out] = bf16(x[T, in] @ Wt[in, out] + b[out]): the Linear with the weight given
+ * transposed, [in, out] row-major (out contiguous; W.t() of an nn.Linear weight made
+ * contiguous, the `nn` layout of "Profiling in PyTorch (Part 2)", section "Where did the
+ * transpose go? Kernel layouts and pre-ops"). No transposed copy is made: the tcgen05 GEMM
+ * reads Wt tiles as an MN-major operand. b may be NULL. in and out multiples of 8 (else
+ * FMLP_ERR_SHAPE), pointers 16-byte aligned, y overlapping no input; one single-SM tcgen05
+ * kernel for every T (no GEMV or few-token variant for this layout). */
+FMLP_API fmlp_status fmlp_linear_bias_wt(const void* x, const void* Wt, const void* b, void* y,
+                                         int64_t T, int64_t in, int64_t out, fmlp_stream_t s);
+
 /* h[T, out] = bf16(act(x[T, in] @ W[out, in]^T + b[out])), act = GELU or ReLU per `mode`, b
  * nullable. The first half of fmlp_mlp_gelu as its own call (bias+activation epilogue). */
 FMLP_API fmlp_status fmlp_linear_bias_gelu(const void* x, const void* W, const void* b, void* h,

@@ -110,6 +110,19 @@ def test_linear_validation(lib):
     assert call_linear(T=0, x=0, y=0) == fm.FMLP_OK
 
 
+def test_transposed_weight_linear_validation(lib):
+    def call(**kw):
+        a = dict(x=A, Wt=A + GB, b=A + 2 * GB, y=A + 3 * GB, T=16, i=32, o=64)
+        a.update(kw)
+        return fm.fmlp_linear_bias_wt(a["x"], a["Wt"], a["b"], a["y"], a["T"], a["i"], a["o"],
+                                      stream=0, raise_on_error=False)
+    assert call(Wt=0) == fm.FMLP_ERR_NULL
+    assert call(i=12) == fm.FMLP_ERR_SHAPE            # the TMA row rule: no padded path here
+    assert call(Wt=A + GB + 8) == fm.FMLP_ERR_ALIGN
+    assert call(y=A + GB + 64) == fm.FMLP_ERR_ALIAS
+    assert call(T=0, x=0, y=0) == fm.FMLP_OK
+
+
 def test_geglu_validation(lib):
     def call(**kw):
         a = dict(x=A, Wg=A + GB, Wu=A + 2 * GB, Wd=A + 3 * GB, y=A + 4 * GB, T=128, D=512,

@@ -530,9 +530,9 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
                  "plan": fm.fmlp_mlp_gelu_plan(T, w.D, w.H, w.Dout),
                  "timing": "CUDA graph of 20 consecutive forwards over 5 rotating weight sets "
                            "(336 MB > 2x L2), replayed 20 times"}
-        if T == 1:
-            ms_stream = events_time(lambda: twenty(stream), 10) / 20
-            entry["us_stream_launched"] = round(ms_stream * 1e3, 2)
+        # raw stream launches (no graph) too
+        ms_stream = events_time(lambda: twenty(stream), 10) / 20
+        entry["us_stream_launched"] = round(ms_stream * 1e3, 2)
         # oracle agreement of the last forward (weight set 4)
         one(stream, 4)
         torch.cuda.synchronize(dev)
@@ -542,6 +542,30 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
             xin, hs["W1"], hs["b1"], hs["W2"], hs["b2"], gelu_mode=oracle.GELU_ERF),
             f"all {T} rows")
         out[f"mlp_4096_t{T}"] = entry
+        if T == 1:
+            # the same forward as the one-kernel decode (both layers in one launch, a grid
+            # barrier between them), which the plans do not choose: measured beside the GEMVs
+            fm.fmlp_test_prefer_decode(1)
+            try:
+                for _ in range(3):
+                    twenty(stream)
+                ms_g = graph_time(torch, dev, twenty, 20) / 20
+                ms_s = events_time(lambda: twenty(stream), 10) / 20
+                one(stream, 4)
+                torch.cuda.synchronize(dev)
+                yk = host(yT)
+            finally:
+                fm.fmlp_test_prefer_decode(0)
+            gk = wbytes / (ms_g * 1e-3) / 1e9
+            out["mlp_4096_t1_one_kernel_decode"] = {
+                "us": round(ms_g * 1e3, 2), "us_stream_launched": round(ms_s * 1e3, 2),
+                "weight_GBps": round(gk, 1), "frac_hbm": round(gk / pk["hbm_gbs"], 4),
+                "plan": fm.FMLP_PLAN_DECODE, "selected_by_default": False,
+                "timing": entry["timing"],
+                "oracle": error_stats(np, yk, oracle.mlp_gelu(
+                    host_sets[4]["x"], host_sets[4]["W1"], host_sets[4]["b1"],
+                    host_sets[4]["W2"], host_sets[4]["b2"], gelu_mode=oracle.GELU_ERF),
+                    "the token")}
     sets.clear()
     host_sets.clear()
 
@@ -564,6 +588,7 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
         for _ in range(2):
             twenty(stream)
         ms_graph = graph_time(torch, dev, twenty, 10) / 20
+        ms_stream = events_time(lambda: twenty(stream), 5) / 20
         wb = 3 * w.D * w.H * 2
         gbs = wb / (ms_graph * 1e-3) / 1e9
         q = dsets[-1]
@@ -571,7 +596,8 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
         torch.cuda.synchronize(dev)
         h = hsets[-1]
         out[name.replace("geglu_8192x", "geglu_decode_t1_")] = {
-            "us": round(ms_graph * 1e3, 2), "weight_GBps": round(gbs, 1),
+            "us": round(ms_graph * 1e3, 2), "us_stream_launched": round(ms_stream * 1e3, 2),
+            "weight_GBps": round(gbs, 1),
             "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "plan": fm.fmlp_geglu_plan(1, w.D, w.H),
             "timing": f"CUDA graph of 20 consecutive one-token forwards over {reps} weight "
                       "set(s), replayed 10 times",

@@ -435,10 +435,21 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
     wsb = fm.fmlp_geglu_workspace_size(w.T, w.D, w.H)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     ms = cold_time(lambda: fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream), 30)
+    kernels = fm.fmlp_describe_plan("geglu", w.T, w.D, w.H)
+    # the same block as two launches (gate/up, then down), which the plan does not choose here
+    fm.fmlp_test_two_stage(-1)
+    try:
+        ms_two = cold_time(
+            lambda: fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream), 30)
+    finally:
+        fm.fmlp_test_two_stage(0)
+    fm.fmlp_geglu(x, Wg, Wu, Wd, y, w.T, w.D, w.H, ws, wsb, stream)
+    torch.cuda.synchronize(dev)
     rows = np.sort(pick.choice(w.T, 256, replace=False))
     out[w.name] = {"ms": round(ms, 4), "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1),
                    "frac_bf16_burst": round(w.flops() / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                   "plan": fm.fmlp_geglu_plan(w.T, w.D, w.H),
+                   "plan": fm.fmlp_geglu_plan(w.T, w.D, w.H), "kernels": kernels,
+                   "ms_two_launches": round(ms_two, 4),
                    "l2": "flushed before every call (median of 30)",
                    "oracle": error_stats(np, host(y)[rows], oracle.geglu(
                        t["x"], t["Wg"], t["Wu"], t["Wd"], rows=rows), "256 seeded rows")}

@@ -15,6 +15,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/fmlp.h"
 #include "internal.h"
@@ -750,6 +751,241 @@ fmlp_status launch_small(const DeviceState& d, bool mlp, const void* x, const vo
   return FMLP_OK;
 }
 
+// Row of per-stream device counters (decode grid barrier, two-stage band counters) that
+// launches on stream s use, or -1 when every row is taken. Launches on one stream run in
+// order, so they can share a row; launches on different streams get different rows.
+int stream_slot(DeviceState& d, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < d.decode_streams; ++i)
+    if (d.decode_stream[i] == s) return i;
+  if (d.decode_streams < kDecodeSlots) {
+    d.decode_stream[d.decode_streams] = s;
+    return d.decode_streams++;
+  }
+  return -1;
+}
+
+// ------------------------------------------------------------------ two-stage block launch
+
+// Both layers of a block in one persistent CTA-pair launch: the pairs work through lists of
+// first-stage tiles and second-stage (down) tiles, so the long down tiles of early bands run
+// while other pairs still compute first-stage tiles, and no pair waits through a partial wave
+// of down tiles at the end, nor for a second launch. Taken when both stages would use the
+// pair kernel and both layers' weights fit in L2 together (the first stage then runs band by
+// band, each band's tiles reading weights that stay resident).
+constexpr double kTwoTileOverhead = 3.0;   // per tile, in 64-deep K steps (prologue, epilogue)
+constexpr int64_t kTwoMaxWeightBytes = 64ll << 20;
+
+struct TwoSchedule {
+  int num_m = 0, num_n1 = 0, num_n2 = 0, kb1 = 0, kb2 = 0, pairs = 0;   // the key
+  std::vector<uint16_t> start, item;
+  double makespan = 0.0;     // estimated, in 64-deep K steps of one pair
+  double two_launch = 0.0;   // the same estimate for two round-robin launches
+};
+
+// List scheduling of the items over the pairs (each pair runs its list in order), in units
+// of one 64-deep K step of a pair. The pair that frees up first takes a down tile whose band
+// is complete while fewer than `early` down tiles have been placed ahead of the last
+// first-stage tile, else the next first-stage tile (band-major order), else the down tile
+// whose band completes first (waiting for it). A down tile is only placed once every
+// first-stage tile of its band has been, so every wait in the lists is on an item placed
+// earlier: with all pairs resident, the waits end. Returns the estimated makespan.
+double list_schedule(const TwoSchedule& sc, int early, std::vector<std::vector<uint16_t>>* lists) {
+  const int num_m = sc.num_m, P = sc.pairs;
+  const int n1 = num_m * sc.num_n1, n2 = num_m * sc.num_n2;
+  const double c1 = sc.kb1 + kTwoTileOverhead, c2 = sc.kb2 + kTwoTileOverhead;
+  lists->assign(P, {});
+  std::vector<double> free_at(P, 0.0), band_ready(num_m, 0.0);
+  std::vector<int> band_left(num_m, sc.num_n1);
+  std::vector<int> pending;   // down items of complete bands, not yet placed
+  int next1 = 0, taken_early = 0;
+  auto band_of = [&](int t) { return (t - n1) / sc.num_n2; };
+  for (int placed = 0; placed < n1 + n2; ++placed) {
+    int p = 0;
+    for (int q = 1; q < P; ++q)
+      if (free_at[q] < free_at[p]) p = q;
+    int best = -1;
+    for (int i = 0; i < static_cast<int>(pending.size()); ++i)
+      if (best < 0 || band_ready[band_of(pending[i])] < band_ready[band_of(pending[best])])
+        best = i;
+    const bool down_now =
+        best >= 0 && taken_early < early && band_ready[band_of(pending[best])] <= free_at[p];
+    if (!down_now && next1 < n1) {
+      const int t = next1++;
+      const int b = t / sc.num_n1;
+      (*lists)[p].push_back(static_cast<uint16_t>(t));
+      free_at[p] += c1;
+      band_ready[b] = std::max(band_ready[b], free_at[p]);
+      if (--band_left[b] == 0)
+        for (int j = 0; j < sc.num_n2; ++j) pending.push_back(n1 + b * sc.num_n2 + j);
+    } else {
+      if (next1 < n1) ++taken_early;
+      const int t = pending[best];
+      pending.erase(pending.begin() + best);
+      (*lists)[p].push_back(static_cast<uint16_t>(t));
+      free_at[p] = std::max(free_at[p], band_ready[band_of(t)]) + c2;
+    }
+  }
+  return *std::max_element(free_at.begin(), free_at.end());
+}
+
+// The schedule with the shortest estimated makespan over a sweep of `early` (the down tiles
+// that do not fill whole waves at the end are the ones worth running early).
+void build_two_schedule(TwoSchedule* sc) {
+  const int n2 = sc->num_m * sc->num_n2;
+  std::vector<std::vector<uint16_t>> lists, best_lists;
+  double best = -1.0;
+  const int step = std::max(1, n2 / 16);
+  for (int e = -1; e <= n2; e += (e < 0 ? 1 : step)) {
+    const int early = e < 0 ? n2 % sc->pairs : e;
+    const double ms = list_schedule(*sc, early, &lists);
+    if (best < 0.0 || ms < best) {
+      best = ms;
+      best_lists.swap(lists);
+    }
+  }
+  sc->start.assign(sc->pairs + 1, 0);
+  sc->item.clear();
+  for (int p = 0; p < sc->pairs; ++p) {
+    sc->item.insert(sc->item.end(), best_lists[p].begin(), best_lists[p].end());
+    sc->start[p + 1] = static_cast<uint16_t>(sc->item.size());
+  }
+  sc->makespan = best;
+  // the same tiles as two round-robin launches over as many pairs, for the automatic choice
+  const int n1 = sc->num_m * sc->num_n1;
+  const double waves1 = (n1 + sc->pairs - 1) / sc->pairs, waves2 = (n2 + sc->pairs - 1) / sc->pairs;
+  sc->two_launch = waves1 * (sc->kb1 + kTwoTileOverhead) + waves2 * (sc->kb2 + kTwoTileOverhead);
+}
+
+// Schedules are a pure function of the key; a few are kept (a model has few block shapes).
+constexpr int kTwoCache = 8;
+std::mutex g_two_mu;
+TwoSchedule g_two_cache[kTwoCache];
+int g_two_next = 0;
+
+// A copy: the cached entry may be replaced by another thread once the lock is released.
+TwoSchedule two_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2, int pairs) {
+  std::lock_guard<std::mutex> lock(g_two_mu);
+  for (const TwoSchedule& c : g_two_cache)
+    if (c.pairs == pairs && c.num_m == num_m && c.num_n1 == num_n1 && c.num_n2 == num_n2 &&
+        c.kb1 == kb1 && c.kb2 == kb2)
+      return c;
+  TwoSchedule& c = g_two_cache[g_two_next];
+  g_two_next = (g_two_next + 1) % kTwoCache;
+  c.num_m = num_m;
+  c.num_n1 = num_n1;
+  c.num_n2 = num_n2;
+  c.kb1 = kb1;
+  c.kb2 = kb2;
+  c.pairs = pairs;
+  build_two_schedule(&c);
+  return c;
+}
+
+// Test hook (fmlp_test_two_stage): 0 automatic, -1 never, 1 whenever the shape is accepted.
+std::atomic<int> g_two_stage{0};
+
+// Pairs of a two-stage launch of this block, or 0 when it does not take one.
+struct TwoPlan {
+  int pairs = 0;
+  int num_m = 0, num_n1 = 0, num_n2 = 0, kb1 = 0, kb2 = 0;
+};
+
+TwoPlan plan_two(const DeviceState& d, int epi1, int64_t T, int64_t D, int64_t H, int64_t Dout) {
+  TwoPlan tp;
+  const int mode = g_two_stage.load(std::memory_order_relaxed);
+  if (mode < 0 || d.max_pairs < 1 || use_skinny(T) || T <= 128 ||
+      g_tile_policy.load(std::memory_order_relaxed) == FMLP_TILES_SINGLE)
+    return tp;
+  const bool geglu = epi1 == EPI_GEGLU;
+  const int64_t w_bytes = static_cast<int64_t>((geglu ? 2 : 1) * mat_bytes(H, D) + mat_bytes(Dout, H));
+  const int64_t num_m = (T + 255) / 256;
+  const int64_t num_n1 = (H + (geglu ? 127 : 255)) / (geglu ? 128 : 256);
+  const int64_t num_n2 = (Dout + 255) / 256;
+  const int64_t items = num_m * (num_n1 + num_n2);
+  if (w_bytes > kTwoMaxWeightBytes || num_m > kTwoMaxBands || items > kTwoMaxItems) return tp;
+  if (mode == 0 && !(choose_gemm(d, epi1, T, H).pair && choose_gemm(d, EPI_BIAS, T, Dout).pair))
+    return tp;
+  const int pairs = std::min(std::min(d.max_pairs, kTwoMaxPairs), static_cast<int>(items));
+  const int kb1 = static_cast<int>((D + 63) / 64), kb2 = static_cast<int>((H + 63) / 64);
+  if (mode == 0) {
+    // only where the list schedule is estimated clearly shorter than two launches
+    const TwoSchedule sc = two_schedule(static_cast<int>(num_m), static_cast<int>(num_n1),
+                                        static_cast<int>(num_n2), kb1, kb2, pairs);
+    if (sc.makespan > 0.95 * sc.two_launch) return tp;
+  }
+  tp.pairs = pairs;
+  tp.num_m = static_cast<int>(num_m);
+  tp.num_n1 = static_cast<int>(num_n1);
+  tp.num_n2 = static_cast<int>(num_n2);
+  tp.kb1 = kb1;
+  tp.kb2 = kb2;
+  return tp;
+}
+
+// One launch for both layers when plan_two accepts the block (*ran = true); otherwise nothing
+// is launched and the caller runs the two GEMMs.
+fmlp_status launch_two(DeviceState& d, int epi1, const void* x, const void* W1a, const void* W1b,
+                       const void* b1, const void* W2, const void* b2, void* h, void* y,
+                       int64_t T, int64_t D, int64_t H, int64_t Dout, int gelu_mode,
+                       cudaStream_t s, int64_t ldx, int64_t ldy, bool* ran) {
+  *ran = false;
+  const TwoPlan tp = plan_two(d, epi1, T, D, H, Dout);
+  if (tp.pairs < 1) return FMLP_OK;
+  const int slot = stream_slot(d, s);
+  if (slot < 0) return FMLP_OK;
+  FMLP_LAUNCH_GUARD("two-stage launch");
+  // test hook: a band count one above what the first stage adds, so every down tile's wait
+  // runs out
+  const bool starve = take_injection(g_inject_skip);
+  const TwoSchedule sc = two_schedule(tp.num_m, tp.num_n1, tp.num_n2, tp.kb1, tp.kb2, tp.pairs);
+  const bool geglu = epi1 == EPI_GEGLU;
+  GemmLaunch L;
+  memset(&L, 0, sizeof L);
+  L.bn = 256;
+  FMLP_TRY(make_map(&L.tmA, x, T, D, 128, "x", ldx));
+  FMLP_TRY(make_map(&L.tmB0, W1a, H, D, 128, geglu ? "Wg" : "W1"));
+  if (geglu) {
+    FMLP_TRY(make_map(&L.tmB1, W1b, H, D, 128, "Wu"));
+  } else {
+    L.tmB1 = L.tmB0;
+  }
+  FMLP_TRY(make_map(&L.tmY, h, T, H, 32, "intermediate"));
+  L.bias = b1;
+  L.M = static_cast<int>(T);
+  L.N_out = static_cast<int>(H);
+  L.K = static_cast<int>(D);
+  L.gelu_mode = gelu_mode;
+  L.epi = epi1;
+  L.pdl = false;
+  L.stream = s;
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
+  if (starve) {
+    const unsigned long long tmo = g_inject_timeout_ns.load(std::memory_order_relaxed);
+    if (tmo) L.timeout_ns = tmo;
+  }
+  L.grid = 2 * tp.pairs;
+  TwoStageLaunch T2;
+  memset(&T2, 0, sizeof T2);
+  FMLP_TRY(make_map(&T2.tmA2, h, T, H, 128, "intermediate"));
+  FMLP_TRY(make_map(&T2.tmB2, W2, Dout, H, 128, geglu ? "Wd" : "W2"));
+  FMLP_TRY(make_map(&T2.tmY2, y, T, Dout, 32, "y", ldy));
+  T2.bias2 = b2;
+  T2.slot = slot;
+  T2.band_extra = starve ? 1 : 0;
+  T2.N2 = static_cast<int>(Dout);
+  T2.K2 = static_cast<int>(H);
+  T2.n1 = tp.num_m * tp.num_n1;
+  T2.n_items = static_cast<int>(sc.item.size());
+  T2.start = sc.start.data();
+  T2.item = sc.item.data();
+  const cudaError_t e = gemm_tc2_two_launch(L, T2);
+  if (e != cudaSuccess) return cuda_fail(e, "two-stage launch");
+  *ran = true;
+  return FMLP_OK;
+}
+
 // One-kernel decode of the whole block. Falls back (returns FMLP_PLAN_NONE in *ran = false)
 // when this device cannot run it or every grid-barrier counter is taken.
 fmlp_status launch_decode(DeviceState& d, bool geglu, const void* x, const void* W1a,
@@ -758,19 +994,7 @@ fmlp_status launch_decode(DeviceState& d, bool geglu, const void* x, const void*
                           int gelu_mode, cudaStream_t s, bool* ran, int64_t ldx, int64_t ldy) {
   *ran = false;
   if (d.decode_occ < 1 || !d.decode_bar) return FMLP_OK;
-  int slot = -1;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    for (int i = 0; i < d.decode_streams; ++i)
-      if (d.decode_stream[i] == s) {
-        slot = i;
-        break;
-      }
-    if (slot < 0 && d.decode_streams < kDecodeSlots) {
-      slot = d.decode_streams++;
-      d.decode_stream[slot] = s;
-    }
-  }
+  const int slot = stream_slot(d, s);
   if (slot < 0) return FMLP_OK;
   FMLP_LAUNCH_GUARD("decode launch");
   DecodeLaunch L;
@@ -1185,8 +1409,11 @@ static fmlp_status geglu_common(const void* x, int64_t ldx, const void* Wg, cons
     if (r == FMLP_OK)
       r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st, 0, ldy);
   } else {
-    r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st, ldx, 0);
-    if (r == FMLP_OK)
+    r = launch_two(*d, EPI_GEGLU, x, Wg, Wu, nullptr, Wd, nullptr, m, y, T, D, H, D, 0, st, ldx,
+                   ldy, &ran);
+    if (r == FMLP_OK && !ran)
+      r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st, ldx, 0);
+    if (r == FMLP_OK && !ran)
       r = launch_gemm(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, D, H, 0, true, st, 0, ldy);
   }
   if (!ws) {
@@ -1424,9 +1651,12 @@ static fmlp_status mlp_common(const void* x, int64_t ldx, const void* W1, const 
     if (r == FMLP_OK)
       r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st, 0, ldy);
   } else {
-    r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D, static_cast<int>(mode),
-                    false, st, ldx, 0);
-    if (r == FMLP_OK)
+    r = launch_two(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, W2, b2, h, y, T, D, H, Dout,
+                   static_cast<int>(mode), st, ldx, ldy, &ran);
+    if (r == FMLP_OK && !ran)
+      r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D,
+                      static_cast<int>(mode), false, st, ldx, 0);
+    if (r == FMLP_OK && !ran)
       r = launch_gemm(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, Dout, H, 0, true, st, 0, ldy);
   }
   if (!ws) {
@@ -1491,11 +1721,24 @@ static std::string describe_decode(const DeviceState& d, const char* name, int64
   char b[256];
   snprintf(b, sizeof b,
            "%s: one weight-streaming kernel for both layers (grid barrier between them), "
-           "T=%lld D=%lld H=%lld Dout=%lld, grid=%d, ring of %d x 32 KB bulk-copy stages",
+           "T=%lld D=%lld H=%lld Dout=%lld, grid=%d, ring of %d bulk-copy stages of whole rows",
            name, static_cast<long long>(T), static_cast<long long>(D), static_cast<long long>(H),
            static_cast<long long>(Dout), d.sms,
            decode_ring_stages(static_cast<int>(T), static_cast<int>(D), static_cast<int>(H),
                               static_cast<int>(Dout), nmat, d.sms));
+  return b;
+}
+
+static std::string describe_two(const TwoPlan& tp, const char* name1, int64_t T, int64_t D,
+                                int64_t H, int64_t Dout) {
+  char b[320];
+  snprintf(b, sizeof b,
+           "%s and down: one tcgen05 CTA-pair launch for both layers, %d first-stage and %d "
+           "down 256-row tiles listed over %d pairs (each band's down tiles after its "
+           "first-stage tiles), T=%lld D=%lld H=%lld Dout=%lld, grid=%d",
+           name1, tp.num_m * tp.num_n1, tp.num_m * tp.num_n2, tp.pairs,
+           static_cast<long long>(T), static_cast<long long>(D), static_cast<long long>(H),
+           static_cast<long long>(Dout), 2 * tp.pairs);
   return b;
 }
 
@@ -1540,6 +1783,8 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += b;
     } else if (p == FMLP_PLAN_GEMV) {
       r += describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
+    } else if (const TwoPlan tp = plan_two(*d, EPI_GEGLU, T, D, H, D); tp.pairs > 0) {
+      r += describe_two(tp, "gate/up", T, D, H, D);
     } else {
       r += describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
            describe_gemm(*d, "down", EPI_BIAS, T, D, H);
@@ -1555,6 +1800,8 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += describe_decode(*d, "MLP block", T, D, H, Dout, 1);
     else if (p == FMLP_PLAN_GEMV)
       r += describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
+    else if (const TwoPlan tp = plan_two(*d, EPI_BIAS_GELU, T, D, H, Dout); tp.pairs > 0)
+      r += describe_two(tp, "up", T, D, H, Dout);
     else
       r += describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
            describe_gemm(*d, "down", EPI_BIAS, T, Dout, H);
@@ -1614,10 +1861,13 @@ fmlp_status fmlp_device_status(fmlp_stream_t s) {
   static const char* sites[] = {"?",          "test wait",          "producer (empty slot)",
                                 "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
                                 "drain",      "fused kernel", "GEMV",
-                                "decode (layer-2 weight copy)", "decode (grid barrier)"};
+                                "decode (layer-2 weight copy)", "decode (grid barrier)",
+                                "two-stage block (band of the intermediate)"};
   const int site = v >> 8;
   set_error("a kernel gave up waiting at: %s (code 0x%x)",
-            (site >= 0 && site < 11) ? sites[site] : "?", v);
+            (site >= 0 && site < static_cast<int>(sizeof sites / sizeof sites[0])) ? sites[site]
+                                                                                     : "?",
+            v);
   return static_cast<fmlp_status>(v & 0xFF);
 }
 
@@ -1667,6 +1917,16 @@ fmlp_status fmlp_test_prefer_decode(int on) {
     return FMLP_ERR_SHAPE;
   }
   g_prefer_decode.store(on, std::memory_order_relaxed);
+  return FMLP_OK;
+}
+
+fmlp_status fmlp_test_two_stage(int mode) {
+  t_last_error.clear();
+  if (mode < -1 || mode > 1) {
+    set_error("mode = %d, expected -1, 0 or 1", mode);
+    return FMLP_ERR_SHAPE;
+  }
+  g_two_stage.store(mode, std::memory_order_relaxed);
   return FMLP_OK;
 }
 

@@ -67,6 +67,27 @@ struct GemmLaunch {
 };
 constexpr int kMoeMaxExperts = 256;
 
+// A whole two-layer block in one persistent CTA-pair launch (gemm_tc2.cu, TWO): the first
+// stage as a GemmLaunch (x, W1 or Wg+Wu, the intermediate as output), the second stage's maps,
+// and the pairs' item lists.
+constexpr int kTwoMaxItems = 2048;
+constexpr int kTwoMaxPairs = 128;
+constexpr int kTwoMaxBands = 64;            // 256-row bands: T up to 16384
+struct TwoStageLaunch {
+  CUtensorMap tmA2;   // the intermediate [M, K2] as A, box {64, 128}
+  CUtensorMap tmB2;   // second-stage weights [N2, K2], box {64, 128}
+  CUtensorMap tmY2;   // output [M, N2], box {64, 32}
+  const void* bias2;  // [N2] or nullptr
+  int slot;           // band-counter row (per stream; launches in one row must not overlap)
+  int band_extra;     // test hook: added to the complete band count (1: never reached)
+  int N2, K2;
+  int n_items;        // items in `item` (first-stage tiles + second-stage tiles)
+  int n1;             // first-stage tiles (band-major numbering), second-stage ones follow
+  const uint16_t* start;   // [pairs + 1]: pair p runs item[start[p] .. start[p + 1])
+  const uint16_t* item;    // [n_items]
+};
+cudaError_t gemm_tc2_two_launch(const GemmLaunch& L, const TwoStageLaunch& T2);
+
 // Few-token tcgen05 GEMM (weights as the MMA's M side, K split over a cluster; gemm_skinny.cu).
 constexpr int kSkinnyMaxT = 128;
 struct SkinnyLaunch {

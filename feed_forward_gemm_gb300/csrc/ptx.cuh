@@ -23,6 +23,7 @@ enum WaitSite : int {
   SITE_GEMV = 8,
   SITE_DECODE_W2 = 9,
   SITE_DECODE_BARRIER = 10,
+  SITE_BAND = 11,
 };
 constexpr int kDeviceTimeoutCode = 7;  // FMLP_ERR_DEVICE_TIMEOUT
 

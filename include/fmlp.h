@@ -101,8 +101,8 @@ typedef enum { FMLP_GELU_TANH = 0, FMLP_GELU_ERF = 1, FMLP_RELU = 2 } fmlp_gelu_
 typedef enum {
     FMLP_PLAN_NONE = 0,         /* T == 0: nothing launched */
     FMLP_PLAN_TC = 1,           /* tcgen05 GEMM kernel(s) (the few-token kernel for 2..128
-                                   tokens, the batched ones above); GeGLU/MLP: 2 kernels,
-                                   m/h in ws */
+                                   tokens, the batched ones above); GeGLU/MLP: 2 kernels, or
+                                   1 two-stage launch (fmlp_test_two_stage), m/h in ws */
     FMLP_PLAN_FUSED_SMALL = 2,  /* GeGLU: whole block in 1 kernel, m kept on chip */
     FMLP_PLAN_GEMV = 3,         /* one token (two when the call's weights are <= 16 MiB):
                                    weight-streaming GEMV kernel(s) */
@@ -322,6 +322,23 @@ FMLP_API fmlp_status fmlp_test_decode_overload(int64_t extra_ctas, int64_t timeo
  * MLP at one token: 19.1 us against 25.4 us). Switch it only while no other thread queries
  * plans or launches. on not 0 or 1: FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
+
+/* Plan switch for the two-stage block launch, process-wide. Under FMLP_PLAN_TC a GeGLU or MLP
+ * block of more than 128 tokens whose weights (both layers) take at most 64 MiB, with at most
+ * 64 bands of 256 tokens and 2048 tiles in all, can run as ONE persistent CTA-pair launch:
+ * the first layer's 256-row tiles and the down tiles share one list per pair, a down tile
+ * waiting (bounded) until every first-layer tile of its 256 rows has been stored. mode 0 (the
+ * default) takes it when both layers would run on the CTA-pair kernel anyway; mode 1 takes it
+ * for every block it accepts (also the FMLP_TILES_PAIR policy's); mode -1 never (two
+ * launches). The results are bit-identical either way: the same tiles, the same K order, the
+ * same roundings. The launch keeps one row of counters per stream, like FMLP_PLAN_DECODE, and
+ * expects every one of its CTA pairs to be resident at once (a concurrent kernel on another
+ * stream that holds SMs until this launch ends makes its waits run out with
+ * FMLP_ERR_DEVICE_TIMEOUT). Under FMLP_INJECT_SKIP_LOAD, a two-stage launch takes the
+ * injection instead as a band count that is never reached, so its down tiles' waits run out.
+ * Switch it only while no other thread queries plans or launches. mode not in {-1, 0, 1}:
+ * FMLP_ERR_SHAPE. */
+FMLP_API fmlp_status fmlp_test_two_stage(int mode);
 
 /* Test hook for the bounded-wait machinery: launches one CTA whose thread waits on an
  * mbarrier that nothing completes, with a limit of timeout_us microseconds (1..2,000,000).

@@ -205,8 +205,8 @@ def test_two_stage_on_row_strided_views(two_stage):
 
 def test_two_stage_band_wait_runs_out(two_stage):
     """A band count one above what the first-layer tiles add: every down tile's wait runs out
-    after 2 ms, the launch records FMLP_ERR_DEVICE_TIMEOUT at the band wait and ends; the
-    counters are back at zero, so the next calls are correct."""
+    after 2 ms, the launch records FMLP_ERR_DEVICE_TIMEOUT and ends; the counters are back at
+    zero, so the next calls are correct."""
     T, D, H = 1000, 512, 1032
     ins = geglu_inputs(T, D, H)
     x, Wg, Wu, Wd = (to_dev(a) for a in ins)
@@ -216,7 +216,10 @@ def test_two_stage_band_wait_runs_out(two_stage):
     fm.fmlp_geglu(x, Wg, Wu, Wd, y, T, D, H, ws, ws.numel())
     torch.cuda.synchronize()
     assert fm.fmlp_device_status() == fm.FMLP_ERR_DEVICE_TIMEOUT
-    assert "band of the intermediate" in fm.fmlp_last_error(), fm.fmlp_last_error()
+    # the first wait to run out records its site: the band wait, or (started a little later,
+    # but polled more often) the MMA's wait for the loads the band wait holds back
+    msg = fm.fmlp_last_error()
+    assert "band of the intermediate" in msg or "MMA (full slot)" in msg, msg
     assert fm.fmlp_device_status() == fm.FMLP_OK
     ref = oracle.geglu(*ins)
     for _ in range(2):

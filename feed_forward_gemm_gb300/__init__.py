@@ -336,7 +336,8 @@ def fmlp_test_prefer_decode(on, raise_on_error=True):
 
 
 def fmlp_test_two_stage(mode, raise_on_error=True):
-    """Two-stage block launch: 0 automatic, 1 whenever accepted, -1 never (process-wide)."""
+    """Two-stage block launch: 0 automatic, 1 whenever accepted, 2 the same with two CTA pairs
+    per cluster sharing operand loads (multicast), -1 never (process-wide)."""
     st = load().fmlp_test_two_stage(int(mode))
     return _check(st, "fmlp_test_two_stage", raise_on_error)
 

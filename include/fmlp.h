@@ -329,14 +329,16 @@ FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
  * the first layer's 256-row tiles and the down tiles share one list per pair, a down tile
  * waiting (bounded) until every first-layer tile of its 256 rows has been stored. mode 0 (the
  * default) takes it when both layers would run on the CTA-pair kernel anyway; mode 1 takes it
- * for every block it accepts (also the FMLP_TILES_PAIR policy's); mode -1 never (two
- * launches). The results are bit-identical either way: the same tiles, the same K order, the
+ * for every block it accepts (also the FMLP_TILES_PAIR policy's); mode 2 the same with two CTA
+ * pairs per 4-CTA cluster running one item list, each pair loading half of the operand the two
+ * share (the x band of a first-layer tile pair, the weight rows of a down tile pair) and
+ * multicasting it to both; mode -1 never (two launches). The results are bit-identical either way: the same tiles, the same K order, the
  * same roundings. The launch keeps one row of counters per stream, like FMLP_PLAN_DECODE, and
  * expects every one of its CTA pairs to be resident at once (a concurrent kernel on another
  * stream that holds SMs until this launch ends makes its waits run out with
  * FMLP_ERR_DEVICE_TIMEOUT). Under FMLP_INJECT_SKIP_LOAD, a two-stage launch takes the
  * injection instead as a band count that is never reached, so its down tiles' waits run out.
- * Switch it only while no other thread queries plans or launches. mode not in {-1, 0, 1}:
+ * Switch it only while no other thread queries plans or launches. mode not in {-1, 0, 1, 2}:
  * FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_two_stage(int mode);
 

@@ -34,13 +34,18 @@
  *     Results are deterministic: no atomics take part in any sum.
  *   - Ownership: all tensor and workspace pointers belong to the caller; the library keeps
  *     none of them after the call returns. The library owns host caches (per device: SM
- *     count, CUDA function attributes, the stream -> barrier-counter table of the decode plan;
- *     per process: encoded TMA tensor maps, keyed by address, sizes, strides and box, so an
- *     entry is valid for any buffer at that address with those sizes), guarded by mutexes, and three arrays of its own device memory on every GPU it runs on,
- *     held until the process exits: the status word below, the decode plan's grid-barrier
- *     counters (1024 x 128 bytes), and the 64 MiB scratch of fmlp_geglu_noalloc. The calls
- *     are thread-safe, with two exceptions stated where they apply: fmlp_geglu_noalloc calls
- *     must not overlap on the GPU, and FMLP_PLAN_DECODE keeps one barrier counter per stream.
+ *     count, CUDA function attributes, the stream -> counter-row table of the decode plan and
+ *     the two-stage block launch; per process: encoded TMA tensor maps, keyed by address,
+ *     sizes, strides and box, so an entry is valid for any buffer at that address with those
+ *     sizes, and the two-stage launches' item lists, keyed by shape), guarded by mutexes, and
+ *     four arrays of its own device memory on every GPU it runs on, held until the process
+ *     exits: the status word below, the decode plan's grid-barrier counters (1024 x 128
+ *     bytes), the two-stage launches' band counters (1024 x 512 bytes), and the 64 MiB
+ *     scratch of fmlp_geglu_noalloc. The calls are thread-safe, with two exceptions stated
+ *     where they apply: fmlp_geglu_noalloc calls must not overlap on the GPU, and
+ *     FMLP_PLAN_DECODE and the two-stage launch keep one row of counters per stream (a launch
+ *     captured in a CUDA graph keeps its stream's row: replays of that graph must not overlap
+ *     one another or other launches on that stream).
  *     The library looks up the device addresses of its arrays once per device; a device reset
  *     (cudaDeviceReset) while the library is loaded leaves them stale and is not supported.
  *   - Requirements checked before anything is launched (the status names the first failure):

@@ -27,6 +27,39 @@ constexpr int kStgBytes = 32 * 128;  // one staging tile: 32 rows x 64 bf16
 constexpr int kEpiWarps = 4;
 constexpr int kStgPerWarp = 2;       // staging tiles per epilogue warp (double buffer)
 
+// a[i] = gelu_tanh(a[i]) * u[i] for 32 values, two at a time (f32x2 arithmetic).
+__device__ __forceinline__ void geglu_pairs(uint32_t (&a)[32], const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint64_t g = f2_pack(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+    const uint64_t m =
+        f2_mul(gelu_tanh_f2(g), f2_pack(__uint_as_float(u[i]), __uint_as_float(u[i + 1])));
+    float m0, m1;
+    f2_unpack(m, m0, m1);
+    a[i] = __float_as_uint(m0);
+    a[i + 1] = __float_as_uint(m1);
+  }
+}
+
+// a[i] = act(a[i]) for 32 values (mode 0 GELU tanh, 1 GELU erf, 2 ReLU), the GELUs two at a
+// time. The mode is chosen once per 32 values, so the evaluations are independent
+// straight-line code the scheduler can overlap.
+__device__ __forceinline__ void act_pairs(uint32_t (&a)[32], int mode) {
+  if (mode == 2) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(relu_f(__uint_as_float(a[i])));
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint64_t v = f2_pack(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+    float y0, y1;
+    f2_unpack(mode == 1 ? gelu_erf_f2(v) : gelu_tanh_f2(v), y0, y1);
+    a[i] = __float_as_uint(y0);
+    a[i + 1] = __float_as_uint(y1);
+  }
+}
+
 // stg: this warp's kStgPerWarp staging tiles; sb: which one is next (kept across tiles).
 template <int BN, int BN_OUT, int EPI>
 __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base, int& sb,
@@ -50,9 +83,7 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
         uint32_t u[32];
         tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
         tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])) * __uint_as_float(u[i]));
+        geglu_pairs(a, u);
       } else {
         tmem_ld_wait();
         const int nb = n_chunk + h * 32;
@@ -71,18 +102,7 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
         }
         // the activation is chosen once per 32 columns, so the 32 evaluations are
         // independent straight-line code the scheduler can overlap
-        if (EPI == EPI_BIAS_GELU) {
-          if (gelu_mode == 1) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_erf_f(__uint_as_float(a[i])));
-          } else if (gelu_mode == 2) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(relu_f(__uint_as_float(a[i])));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])));
-          }
-        }
+        if (EPI == EPI_BIAS_GELU) act_pairs(a, gelu_mode);
       }
       // 32 values = 4 x 16 bytes; 16-byte chunk j of this row goes to slot j ^ (row & 7)
 #pragma unroll
@@ -127,9 +147,7 @@ __device__ __forceinline__ void epilogue_rows_direct(uint32_t t_row, int lane, b
       uint32_t u[32];
       tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
       tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        a[i] = __float_as_uint(gelu_tanh_f(__uint_as_float(a[i])) * __uint_as_float(u[i]));
+      geglu_pairs(a, u);
     } else {
       tmem_ld_wait();
       const int nb = n_tile0 + c;
@@ -146,11 +164,7 @@ __device__ __forceinline__ void epilogue_rows_direct(uint32_t t_row, int lane, b
           a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
         }
       }
-      if (EPI == EPI_BIAS_GELU) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          a[i] = __float_as_uint(gelu_f(__uint_as_float(a[i]), gelu_mode));
-      }
+      if (EPI == EPI_BIAS_GELU) act_pairs(a, gelu_mode);
     }
     if (row_ok) {
 #pragma unroll

@@ -779,6 +779,9 @@ int stream_slot(DeviceState& d, cudaStream_t s) {
 // pair kernel and both layers' weights fit in L2 together (the first stage then runs band by
 // band, each band's tiles reading weights that stay resident).
 constexpr double kTwoTileOverhead = 3.0;   // per tile, in 64-deep K steps (prologue, epilogue)
+// Bands per group of the first stage's order (GPT-2-small block, groups of 1/2/4/8/16/32:
+// 81.9/79.7/78.8/78.1/79.9/84.0 us).
+constexpr int kTwoGroup = 8;
 constexpr int64_t kTwoMaxWeightBytes = 64ll << 20;
 
 struct TwoSchedule {
@@ -793,12 +796,13 @@ struct TwoSchedule {
 // List scheduling of the items over the lists (each list runs in order on its pair, or its two
 // pairs), in units of one 64-deep K step. The list that frees up first takes a down item whose
 // bands are complete while fewer than `early` down items have been placed ahead of the last
-// first-stage item, else the next first-stage item (band-major order), else the down item
+// first-stage item, else the next first-stage item, else the down item
 // whose bands complete first (waiting for them). A down item is only placed once every
 // first-stage item of its bands has been, so every wait in the lists is on an item placed
 // earlier: with all pairs resident, the waits end. Returns the estimated makespan.
-// Items: first stage u = band * per1 + j (per1 = N tiles, or N tile pairs when mc = 2), then
-// down items n1 + group * num_n2 + n, a group being one band (or two when mc = 2).
+// Items: first stage u = band * per1 + j (per1 = N tiles, or N tile pairs when mc = 2), taken
+// in groups of kTwoGroup bands with the band running fastest; then down items
+// n1 + group * num_n2 + n, a group being one band (or two when mc = 2).
 double list_schedule(const TwoSchedule& sc, int early, std::vector<std::vector<uint16_t>>* lists) {
   const int num_m = sc.num_m, P = sc.lists, mc = sc.mc;
   const int per1 = mc == 2 ? (sc.num_n1 + 1) / 2 : sc.num_n1;
@@ -823,7 +827,11 @@ double list_schedule(const TwoSchedule& sc, int early, std::vector<std::vector<u
     const bool down_now =
         best >= 0 && taken_early < early && group_ready[group_of(pending[best])] <= free_at[p];
     if (!down_now && next1 < n1) {
-      const int t = next1++;
+      // first-stage items in groups of kTwoGroup bands, the band running fastest, so the
+      // pairs in flight read each weight tile at about the same time from L2
+      const int k = next1++, per_group = kTwoGroup * per1, kg = k / per_group;
+      const int r = k - kg * per_group, gb = std::min(kTwoGroup, num_m - kg * kTwoGroup);
+      const int t = (kg * kTwoGroup + r % gb) * per1 + r / gb;
       const int b = t / per1, g = b / mc;
       (*lists)[p].push_back(static_cast<uint16_t>(t));
       free_at[p] += c1;

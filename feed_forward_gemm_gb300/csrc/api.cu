@@ -938,10 +938,11 @@ TwoPlan plan_two(const DeviceState& d, int epi1, int64_t T, int64_t D, int64_t H
                              static_cast<int>(items));
   const int kb1 = static_cast<int>((D + 63) / 64), kb2 = static_cast<int>((H + 63) / 64);
   if (mode == 0) {
-    // only where the list schedule is estimated clearly shorter than two launches
+    // only where the list schedule is estimated clearly shorter than two launches (at 0.92
+    // of their estimate a 8192x1024x4096 GeGLU block measured 2.6 % slower in one launch)
     const TwoSchedule sc = two_schedule(static_cast<int>(num_m), static_cast<int>(num_n1),
                                         static_cast<int>(num_n2), kb1, kb2, lists, mc);
-    if (sc.makespan > 0.95 * sc.two_launch) return tp;
+    if (sc.makespan > 0.9 * sc.two_launch) return tp;
   }
   tp.lists = lists;
   tp.mc = mc;

@@ -27,6 +27,29 @@ constexpr int kStgBytes = 32 * 128;  // one staging tile: 32 rows x 64 bf16
 constexpr int kEpiWarps = 4;
 constexpr int kStgPerWarp = 2;       // staging tiles per epilogue warp (double buffer)
 
+// a[i] += b[n0 + i] for 32 columns (b = 0 past N_out or without a bias: the +0 still turns an
+// accumulator of -0 into +0, as a sum that starts from zero does), two at a time.
+__device__ __forceinline__ void bias_pairs(uint32_t (&a)[32], const __nv_bfloat16* __restrict__ bias,
+                                           int n0, int N_out) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (bias != nullptr && n0 + q * 8 < N_out)
+      w = __ldg(reinterpret_cast<const uint4*>(bias + n0 + q * 8));
+    const uint32_t wb[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = q * 8 + e * 2;
+      float s0, s1;
+      f2_unpack(f2_add(f2_pack(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                       f2_pack(bf16_lo(wb[e]), bf16_hi(wb[e]))),
+                s0, s1);
+      a[i] = __float_as_uint(s0);
+      a[i + 1] = __float_as_uint(s1);
+    }
+  }
+}
+
 // a[i] = gelu_tanh(a[i]) * u[i] for 32 values, two at a time (f32x2 arithmetic).
 __device__ __forceinline__ void geglu_pairs(uint32_t (&a)[32], const uint32_t (&u)[32]) {
 #pragma unroll
@@ -86,20 +109,7 @@ __device__ __forceinline__ void epilogue_cols(uint32_t t_row, uint8_t* stg_base,
         geglu_pairs(a, u);
       } else {
         tmem_ld_wait();
-        const int nb = n_chunk + h * 32;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (bias != nullptr && nb + q * 8 < N_out)
-            w = __ldg(reinterpret_cast<const uint4*>(bias + nb + q * 8));
-          const uint32_t wb[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = q * 8 + e * 2;
-            a[i] = __float_as_uint(__uint_as_float(a[i]) + bf16_lo(wb[e]));
-            a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
-          }
-        }
+        bias_pairs(a, bias, n_chunk + h * 32, N_out);
         // the activation is chosen once per 32 columns, so the 32 evaluations are
         // independent straight-line code the scheduler can overlap
         if (EPI == EPI_BIAS_GELU) act_pairs(a, gelu_mode);
@@ -150,20 +160,7 @@ __device__ __forceinline__ void epilogue_rows_direct(uint32_t t_row, int lane, b
       geglu_pairs(a, u);
     } else {
       tmem_ld_wait();
-      const int nb = n_tile0 + c;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (bias != nullptr && nb + q * 8 < N_out)
-          w = __ldg(reinterpret_cast<const uint4*>(bias + nb + q * 8));
-        const uint32_t wb[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = q * 8 + e * 2;
-          a[i] = __float_as_uint(__uint_as_float(a[i]) + bf16_lo(wb[e]));
-          a[i + 1] = __float_as_uint(__uint_as_float(a[i + 1]) + bf16_hi(wb[e]));
-        }
-      }
+      bias_pairs(a, bias, n_tile0 + c, N_out);
       if (EPI == EPI_BIAS_GELU) act_pairs(a, gelu_mode);
     }
     if (row_ok) {

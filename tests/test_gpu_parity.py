@@ -133,6 +133,43 @@ def test_linear_bias_gelu_vs_oracle(mode, T, K, N):
     assert_parity(to_host(h), ref_h, "linear+bias+activation")
 
 
+# values whose activation is fixed exactly in bf16 (no tail of the approximations involved)
+SPECIALS = [np.inf, -np.inf, np.nan, 3.0e38, -3.0e38, 1e30, -1e30, 0.0, -0.0, 100.0, -100.0,
+            1e-30, -1e-30]
+
+
+@pytest.mark.parametrize("mode", [fm.FMLP_GELU_TANH, fm.FMLP_GELU_ERF, fm.FMLP_RELU])
+@pytest.mark.parametrize("T,policy", [(512, fm.FMLP_TILES_PAIR), (512, fm.FMLP_TILES_SINGLE),
+                                      (40, fm.FMLP_TILES_AUTO)])
+def test_activation_special_values_through_the_epilogues(mode, T, policy):
+    """x = 0 and W = 0, so the pre-activation is the bias exactly: infinities, NaN, the bf16
+    extremes, +-0 and values deep in either tail, through the CTA-pair, single-SM and
+    few-token epilogues. Each output is the oracle's bf16 of act(0 + b), bit for bit (NaN as
+    NaN; -inf gives NaN in both GELU forms, as the formula evaluated in IEEE arithmetic)."""
+    K, N = 64, 1024
+    vals = np.array(SPECIALS * (N // len(SPECIALS) + 1))[:N]
+    b = np.array([oracle.round_bf16(float(v)) for v in vals], np.uint16)
+    x = np.zeros((T, K), np.uint16)
+    W = np.zeros((N, K), np.uint16)
+    h = empty_bf16(T, N)
+    fm.fmlp_set_tile_policy(policy)
+    try:
+        fm.fmlp_linear_bias_gelu(to_dev(x), to_dev(W), to_dev(b), h, T, K, N, mode)
+        torch.cuda.synchronize()
+    finally:
+        fm.fmlp_set_tile_policy(fm.FMLP_TILES_AUTO)
+    got = to_host(h)
+    omode = {0: oracle.GELU_TANH, 1: oracle.GELU_ERF, 2: oracle.RELU}[mode]
+    ref = np.array([oracle.round_bf16(float(v)) for v in
+                    oracle.gelu(bits_to_f64(b).astype(np.float64) + 0.0, omode)], np.uint16)
+    ref = np.broadcast_to(ref, got.shape)
+    gnan, rnan = np.isnan(bits_to_f64(got)), np.isnan(bits_to_f64(ref))
+    assert np.array_equal(gnan, rnan), (vals[np.flatnonzero(gnan[0] != rnan[0])[:5]])
+    bad = np.flatnonzero((got[0] != ref[0]) & ~rnan[0])
+    assert bad.size == 0, [(vals[i], hex(got[0, i]), hex(ref[0, i])) for i in bad[:6]]
+    assert np.array_equal(got[:, ~rnan[0]], ref[:, ~rnan[0]])
+
+
 # ------------------------------------------------------------------------ GeGLU
 
 GEGLU_SHAPES = [(1, 32, 64), (3, 64, 128), (129, 32, 64), (200, 136, 264), (300, 192, 320),

@@ -32,6 +32,7 @@ __all__ = [
     "FMLP_PLAN_FUSED_SMALL", "FMLP_PLAN_GEMV", "FMLP_PLAN_DECODE", "fmlp_test_decode_overload",
     "fmlp_test_prefer_decode",
     "fmlp_test_two_stage",
+    "fmlp_test_fewtoken_block",
     "fmlp_test_inject", "FMLP_INJECT_NONE", "FMLP_INJECT_LAUNCH", "FMLP_INJECT_SKIP_LOAD",
 ]
 
@@ -76,6 +77,7 @@ _SIGNATURES = {
     "fmlp_test_decode_overload": (_INT, [_I64, _I64]),
     "fmlp_test_prefer_decode": (_INT, [_INT]),
     "fmlp_test_two_stage": (_INT, [_INT]),
+    "fmlp_test_fewtoken_block": (_INT, [_INT]),
     "fmlp_test_inject": (_INT, [_INT, _I64, _I64]),
     "fmlp_status_string": (ctypes.c_char_p, [_INT]),
     "fmlp_last_error": (ctypes.c_char_p, []),
@@ -340,6 +342,12 @@ def fmlp_test_two_stage(mode, raise_on_error=True):
     per cluster sharing operand loads (multicast), -1 never (process-wide)."""
     st = load().fmlp_test_two_stage(int(mode))
     return _check(st, "fmlp_test_two_stage", raise_on_error)
+
+
+def fmlp_test_fewtoken_block(mode, raise_on_error=True):
+    """Few-token block in one launch: 0 automatic, 1 whenever accepted, -1 never."""
+    st = load().fmlp_test_fewtoken_block(int(mode))
+    return _check(st, "fmlp_test_fewtoken_block", raise_on_error)
 
 
 def fmlp_test_wait_timeout(timeout_us, stream=None, raise_on_error=True):

@@ -54,6 +54,9 @@ struct DeviceState {
   int max_quads = 0;   // co-resident 4-CTA clusters of the multicast two-stage kernel
   // co-resident clusters of 1, 2, 4, 8 few-token CTAs (0: unknown, assume sms / size)
   int skinny_clusters[4] = {0, 0, 0, 0};
+  // co-resident clusters of 1, 2, 4, 8 CTAs of the few-token block kernel (0: unknown: the
+  // one-launch block is not taken)
+  int fewblock_clusters[4] = {0, 0, 0, 0};
   int* status = nullptr;
   int decode_occ = 0;  // resident decode CTAs per SM (0: the one-kernel decode cannot run)
   unsigned long long* decode_bar = nullptr;  // grid-barrier counters (kDecodeSlots)
@@ -149,6 +152,10 @@ fmlp_status device_state(DeviceState** out) {
     for (int i = 0; i < 4; ++i) {
       if (gemm_skinny_max_clusters(1 << i, &d.skinny_clusters[i]) != cudaSuccess) {
         d.skinny_clusters[i] = 0;
+        (void)cudaGetLastError();
+      }
+      if (fewtoken_block_max_clusters(1 << i, &d.fewblock_clusters[i]) != cudaSuccess) {
+        d.fewblock_clusters[i] = 0;
         (void)cudaGetLastError();
       }
     }
@@ -1023,6 +1030,101 @@ fmlp_status launch_two(DeviceState& d, int epi1, const void* x, const void* W1a,
   return FMLP_OK;
 }
 
+// ------------------------------------------------------------ few-token block launch
+
+// Test hook (fmlp_test_fewtoken_block): 0 automatic, 1 whenever the shape is accepted, -1 never.
+std::atomic<int> g_fewblock{0};
+
+struct FewBlockPlan {
+  bool ok = false;
+  int rows1 = 0, rows2 = 0, tiles = 0, split = 0, tpad = 0;
+};
+
+// Both layers of a few-token block in one launch: the few-token kernel's tiling of layer 1,
+// the same tiles and K split for layer 2, every CTA resident at once, the ring and the
+// exchange region within one CTA's shared memory.
+FewBlockPlan plan_fewblock(const DeviceState& d, int epi1, int64_t T, int64_t D, int64_t H,
+                           int64_t Dout) {
+  FewBlockPlan p;
+  const int mode = g_fewblock.load(std::memory_order_relaxed);
+  if (mode < 0 || !use_skinny(T) || !d.decode_bar) return p;
+  const int nmat1 = epi1 == EPI_GEGLU ? 2 : 1;
+  const int64_t tpad = (T + 31) / 32 * 32;
+  if (tpad > (nmat1 == 2 ? 64 : 128)) return p;
+  const SkinnyShape sh = skinny_shape(d, H, D, tpad);
+  const int64_t rows2 = ((Dout + sh.tiles - 1) / sh.tiles + 3) / 4 * 4;
+  if (sh.rows > 128 || rows2 > 128 || sh.split > (D + 63) / 64 || sh.split > (H + 63) / 64)
+    return p;
+  int si = 0;
+  while ((1 << si) < sh.split) ++si;
+  if (sh.tiles > d.fewblock_clusters[si]) return p;   // every CTA must be resident at once
+  if (fewtoken_block_stages(nmat1, static_cast<int>(tpad), sh.split, sh.rows,
+                            static_cast<int>(rows2), nullptr, nullptr) == 0)
+    return p;
+  // Automatically only where it measured faster (CUDA graphs of 20 forwards, rotating weights):
+  // layer 2's tiles at least half as tall as layer 1's and at most 64 tokens. The 4096-wide MLP
+  // at 2/16/64 tokens took 19.7/19.7/22.5 us in one launch against 20.7/21.1/23.1 in two; at
+  // 128 tokens 26.6 against 26.0; the GPT-2-small GeGLU block (layer-2 tiles of 24 rows against
+  // 88) 13.7 against 11.8 at 16 tokens.
+  if (mode == 0 && (tpad > 64 || 2 * rows2 < sh.rows)) return p;
+  p.ok = true;
+  p.rows1 = sh.rows;
+  p.rows2 = static_cast<int>(rows2);
+  p.tiles = sh.tiles;
+  p.split = sh.split;
+  p.tpad = static_cast<int>(tpad);
+  return p;
+}
+
+fmlp_status launch_fewblock(DeviceState& d, int epi1, const void* x, const void* W1a,
+                            const void* W1b, const void* b1, const void* W2, const void* b2,
+                            void* h, void* y, int64_t T, int64_t D, int64_t H, int64_t Dout,
+                            int gelu_mode, cudaStream_t s, int64_t ldx, int64_t ldy, bool* ran) {
+  *ran = false;
+  const FewBlockPlan p = plan_fewblock(d, epi1, T, D, H, Dout);
+  if (!p.ok) return FMLP_OK;
+  const int slot = stream_slot(d, s);
+  if (slot < 0) return FMLP_OK;
+  FMLP_LAUNCH_GUARD("few-token block launch");
+  const bool geglu = epi1 == EPI_GEGLU;
+  FewBlockLaunch L;
+  memset(&L, 0, sizeof L);
+  FMLP_TRY(make_map(&L.tmW1a, W1a, H, D, static_cast<uint32_t>(p.rows1), geglu ? "Wg" : "W1"));
+  if (geglu) {
+    FMLP_TRY(make_map(&L.tmW1b, W1b, H, D, static_cast<uint32_t>(p.rows1), "Wu"));
+  } else {
+    L.tmW1b = L.tmW1a;
+  }
+  FMLP_TRY(make_map(&L.tmX, x, T, D, static_cast<uint32_t>(p.tpad), "x", ldx));
+  FMLP_TRY(make_map(&L.tmW2, W2, Dout, H, static_cast<uint32_t>(p.rows2), geglu ? "Wd" : "W2"));
+  FMLP_TRY(make_map(&L.tmH, h, T, H, static_cast<uint32_t>(p.tpad), "intermediate"));
+  L.b1 = b1;
+  L.b2 = b2;
+  L.h = h;
+  L.y = y;
+  L.barrier = d.decode_bar + 16 * slot;
+  L.T = static_cast<int>(T);
+  L.D = static_cast<int>(D);
+  L.H = static_cast<int>(H);
+  L.Dout = static_cast<int>(Dout);
+  L.ldy = static_cast<int>(ldy > 0 ? ldy : Dout);
+  L.tpad = p.tpad;
+  L.rows1 = p.rows1;
+  L.rows2 = p.rows2;
+  L.tiles = p.tiles;
+  L.split = p.split;
+  L.epi1 = epi1;
+  L.gelu_mode = gelu_mode;
+  L.pdl = true;
+  L.stream = s;
+  L.status = d.status;
+  L.timeout_ns = kWaitTimeoutNs;
+  const cudaError_t e = fewtoken_block_launch(L);
+  if (e != cudaSuccess) return cuda_fail(e, "few-token block launch");
+  *ran = true;
+  return FMLP_OK;
+}
+
 // One-kernel decode of the whole block. Falls back (returns FMLP_PLAN_NONE in *ran = false)
 // when this device cannot run it or every grid-barrier counter is taken.
 fmlp_status launch_decode(DeviceState& d, bool geglu, const void* x, const void* W1a,
@@ -1446,8 +1548,11 @@ static fmlp_status geglu_common(const void* x, int64_t ldx, const void* Wg, cons
     if (r == FMLP_OK)
       r = launch_gemv(*d, EPI_BIAS, m, Wd, nullptr, nullptr, y, T, H, D, 0, st, 0, ldy);
   } else {
-    r = launch_two(*d, EPI_GEGLU, x, Wg, Wu, nullptr, Wd, nullptr, m, y, T, D, H, D, 0, st, ldx,
-                   ldy, &ran);
+    r = launch_fewblock(*d, EPI_GEGLU, x, Wg, Wu, nullptr, Wd, nullptr, m, y, T, D, H, D, 0, st,
+                        ldx, ldy, &ran);
+    if (r == FMLP_OK && !ran)
+      r = launch_two(*d, EPI_GEGLU, x, Wg, Wu, nullptr, Wd, nullptr, m, y, T, D, H, D, 0, st,
+                     ldx, ldy, &ran);
     if (r == FMLP_OK && !ran)
       r = launch_gemm(*d, EPI_GEGLU, x, Wg, Wu, nullptr, m, T, H, D, 0, false, st, ldx, 0);
     if (r == FMLP_OK && !ran)
@@ -1688,8 +1793,11 @@ static fmlp_status mlp_common(const void* x, int64_t ldx, const void* W1, const 
     if (r == FMLP_OK)
       r = launch_gemv(*d, EPI_BIAS, h, W2, nullptr, b2, y, T, H, Dout, 0, st, 0, ldy);
   } else {
-    r = launch_two(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, W2, b2, h, y, T, D, H, Dout,
-                   static_cast<int>(mode), st, ldx, ldy, &ran);
+    r = launch_fewblock(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, W2, b2, h, y, T, D, H, Dout,
+                        static_cast<int>(mode), st, ldx, ldy, &ran);
+    if (r == FMLP_OK && !ran)
+      r = launch_two(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, W2, b2, h, y, T, D, H, Dout,
+                     static_cast<int>(mode), st, ldx, ldy, &ran);
     if (r == FMLP_OK && !ran)
       r = launch_gemm(*d, EPI_BIAS_GELU, x, W1, nullptr, b1, h, T, H, D,
                       static_cast<int>(mode), false, st, ldx, 0);
@@ -1766,6 +1874,20 @@ static std::string describe_decode(const DeviceState& d, const char* name, int64
   return b;
 }
 
+static std::string describe_fewblock(const FewBlockPlan& p, const char* name1, int64_t T,
+                                     int64_t D, int64_t H, int64_t Dout) {
+  char b[384];
+  snprintf(b, sizeof b,
+           "%s and down: one few-token tcgen05 launch for both layers (weights as the M side, "
+           "%d + %d weight rows x %d tokens per tile, K split %d ways over a cluster, layer 2's "
+           "weights prefetched before a grid barrier on h), T=%lld D=%lld H=%lld Dout=%lld, "
+           "grid=%d",
+           name1, p.rows1, p.rows2, p.tpad, p.split, static_cast<long long>(T),
+           static_cast<long long>(D), static_cast<long long>(H), static_cast<long long>(Dout),
+           p.tiles * p.split);
+  return b;
+}
+
 static std::string describe_two(const TwoPlan& tp, const char* name1, int64_t T, int64_t D,
                                 int64_t H, int64_t Dout) {
   char b[384];
@@ -1821,6 +1943,8 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += b;
     } else if (p == FMLP_PLAN_GEMV) {
       r += describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
+    } else if (const FewBlockPlan fp = plan_fewblock(*d, EPI_GEGLU, T, D, H, D); fp.ok) {
+      r += describe_fewblock(fp, "gate/up", T, D, H, D);
     } else if (const TwoPlan tp = plan_two(*d, EPI_GEGLU, T, D, H, D); tp.lists > 0) {
       r += describe_two(tp, "gate/up", T, D, H, D);
     } else {
@@ -1838,6 +1962,8 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += describe_decode(*d, "MLP block", T, D, H, Dout, 1);
     else if (p == FMLP_PLAN_GEMV)
       r += describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
+    else if (const FewBlockPlan fp = plan_fewblock(*d, EPI_BIAS_GELU, T, D, H, Dout); fp.ok)
+      r += describe_fewblock(fp, "up", T, D, H, Dout);
     else if (const TwoPlan tp = plan_two(*d, EPI_BIAS_GELU, T, D, H, Dout); tp.lists > 0)
       r += describe_two(tp, "up", T, D, H, Dout);
     else
@@ -1900,7 +2026,8 @@ fmlp_status fmlp_device_status(fmlp_stream_t s) {
                                 "MMA (full slot)", "MMA (free accumulator)", "epilogue (accumulator)",
                                 "drain",      "fused kernel", "GEMV",
                                 "decode (layer-2 weight copy)", "decode (grid barrier)",
-                                "two-stage block (band of the intermediate)"};
+                                "two-stage block (band of the intermediate)",
+                                "few-token block (grid barrier)"};
   const int site = v >> 8;
   set_error("a kernel gave up waiting at: %s (code 0x%x)",
             (site >= 0 && site < static_cast<int>(sizeof sites / sizeof sites[0])) ? sites[site]
@@ -1955,6 +2082,16 @@ fmlp_status fmlp_test_prefer_decode(int on) {
     return FMLP_ERR_SHAPE;
   }
   g_prefer_decode.store(on, std::memory_order_relaxed);
+  return FMLP_OK;
+}
+
+fmlp_status fmlp_test_fewtoken_block(int mode) {
+  t_last_error.clear();
+  if (mode < -1 || mode > 1) {
+    set_error("mode = %d, expected -1, 0 or 1", mode);
+    return FMLP_ERR_SHAPE;
+  }
+  g_fewblock.store(mode, std::memory_order_relaxed);
   return FMLP_OK;
 }
 

@@ -115,6 +115,33 @@ struct SkinnyLaunch {
 };
 cudaError_t gemm_skinny_launch(const SkinnyLaunch& L);
 
+// Both layers of a few-token block in one launch (fewtoken_block.cu): layer 1 (x, W1 or
+// Wg+Wu, bias1 + activation, or the GeGLU product) to h, a grid barrier, layer 2 (h, W2,
+// bias2) to y, with the tiling of the few-token kernel shared by both layers (the same tiles
+// and K split: rows1 and rows2 weight rows per tile).
+struct FewBlockLaunch {
+  CUtensorMap tmW1a, tmW1b;   // layer 1 weights [H, D], box {64, rows1}
+  CUtensorMap tmX;            // x [T, D], box {64, tpad}
+  CUtensorMap tmW2;           // layer 2 weights [Dout, H], box {64, rows2}
+  CUtensorMap tmH;            // h [T, H], box {64, tpad}
+  const void* b1;             // [H] or nullptr (GeGLU: unused)
+  const void* b2;             // [Dout] or nullptr
+  void* h;                    // [T, H] bf16 (the caller's workspace)
+  void* y;                    // [T, Dout] bf16, row stride ldy
+  unsigned long long* barrier;   // grid-barrier counter (shared with the decode plan's row)
+  int T, D, H, Dout, ldy, tpad, rows1, rows2, tiles, split, epi1, gelu_mode;
+  bool pdl;
+  cudaStream_t stream;
+  int* status;
+  uint64_t timeout_ns;
+};
+cudaError_t fewtoken_block_launch(const FewBlockLaunch& L);
+// Clusters of `split` CTAs of the few-token block kernel that can be resident at once.
+cudaError_t fewtoken_block_max_clusters(int split, int* clusters);
+// Ring stages of the launch (0: it does not fit), its shared memory and exchange-region bytes.
+int fewtoken_block_stages(int nmat1, int tpad, int split, int rows1, int rows2, int* smem_out,
+                          int* xbytes_out);
+
 // Zero-padded copies (pad.cu): dst [dst_rows, dst_cols] (dst_cols a multiple of 8) takes
 // src [rows, cols] (row stride ld) and zeros elsewhere; copy2d copies rows x cols between
 // row strides.

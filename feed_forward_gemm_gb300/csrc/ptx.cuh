@@ -24,6 +24,7 @@ enum WaitSite : int {
   SITE_DECODE_W2 = 9,
   SITE_DECODE_BARRIER = 10,
   SITE_BAND = 11,
+  SITE_FEWBLOCK_BARRIER = 12,
 };
 constexpr int kDeviceTimeoutCode = 7;  // FMLP_ERR_DEVICE_TIMEOUT
 

@@ -347,6 +347,20 @@ FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
  * FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_two_stage(int mode);
 
+/* Plan switch for the few-token block launch, process-wide. Under FMLP_PLAN_TC a GeGLU block
+ * of 2..64 tokens, or an MLP block of 2..128, can run both layers in ONE launch of the
+ * few-token kernel's design (weights as the MMA's M side, K split over a cluster): layer 1 to
+ * h in the workspace, layer 2's first weight tiles prefetched into shared memory meanwhile, a
+ * bounded grid barrier (a counter of the stream's decode-plan row) before h is read, layer 2
+ * to y. It needs every CTA resident at once (a concurrent kernel on another stream that holds
+ * SMs until this launch ends makes its barrier run out with FMLP_ERR_DEVICE_TIMEOUT). mode 0
+ * (the default) takes it for blocks of at most 64 tokens whose second layer's weight tiles
+ * are at least half as tall as the first's (e.g. the 4096-wide MLP; measured faster there,
+ * slower otherwise); 1 takes it for every block it accepts; -1 never (two few-token launches). Results agree with the two launches within rounding (the same tiles,
+ * K slices and slice order). Switch it only while no other thread queries plans or launches.
+ * mode not in {-1, 0, 1}: FMLP_ERR_SHAPE. */
+FMLP_API fmlp_status fmlp_test_fewtoken_block(int mode);
+
 /* Test hook for the bounded-wait machinery: launches one CTA whose thread waits on an
  * mbarrier that nothing completes, with a limit of timeout_us microseconds (1..2,000,000).
  * The kernel then records FMLP_ERR_DEVICE_TIMEOUT and exits; nothing faults or hangs. */

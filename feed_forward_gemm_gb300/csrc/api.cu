@@ -1111,14 +1111,18 @@ fmlp_status launch_fewblock(DeviceState& d, int epi1, const void* x, const void*
   L.tpad = p.tpad;
   L.rows1 = p.rows1;
   L.rows2 = p.rows2;
-  L.tiles = p.tiles;
+  // test hook (fmlp_test_decode_overload): clusters beyond the resident ones, whose tiles lie
+  // past the last weight row (zero-filled loads, no stores), so the barrier's wait runs out
+  const int extra = g_decode_extra_ctas.load(std::memory_order_relaxed);
+  L.tiles = p.tiles + (extra + p.split - 1) / p.split;
   L.split = p.split;
   L.epi1 = epi1;
   L.gelu_mode = gelu_mode;
   L.pdl = true;
   L.stream = s;
   L.status = d.status;
-  L.timeout_ns = kWaitTimeoutNs;
+  const unsigned long long tmo = g_decode_timeout_ns.load(std::memory_order_relaxed);
+  L.timeout_ns = tmo ? tmo : kWaitTimeoutNs;
   const cudaError_t e = fewtoken_block_launch(L);
   if (e != cudaSuccess) return cuda_fail(e, "few-token block launch");
   *ran = true;

@@ -406,8 +406,10 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       uint32_t hphase = 0;   // bit i: parity of stage i's next h fill
       for (int kb = k2_0; kb < k2_1; ++kb) {
         if (!mbar_wait(&full[mstage], mphase, a.status, SITE_MMA_FULL, a.timeout_ns)) break;
+        // the first h tile comes only after the grid barrier: that wait gets the barrier's
+        // limit on top of its own, so a barrier that runs out is the site recorded
         if (!mbar_wait(&hfull[mstage], (hphase >> mstage) & 1u, a.status, SITE_MMA_FULL,
-                       a.timeout_ns))
+                       kb == k2_0 ? 2 * a.timeout_ns : a.timeout_ns))
           break;
         hphase ^= 1u << mstage;
         tc_fence_after();

@@ -311,8 +311,10 @@ typedef enum {
 } fmlp_inject_kind;
 FMLP_API fmlp_status fmlp_test_inject(int kind, int64_t count, int64_t timeout_us);
 
-/* Test hook for the one-kernel decode plan (FMLP_PLAN_DECODE), process-wide: later decode
- * launches add extra_ctas CTAs beyond the ones that can be resident at once, so the resident
+/* Test hook for the launches with a grid barrier, process-wide: later one-kernel decode
+ * launches (FMLP_PLAN_DECODE) and few-token block launches (fmlp_test_fewtoken_block) add
+ * extra_ctas CTAs (the latter: rounded up to whole clusters, their tiles past the last weight
+ * row) beyond the ones that can be resident at once, so the resident
  * CTAs wait at the grid barrier for CTAs that cannot start until they leave, and every device
  * wait of those launches is bounded by timeout_us (0: the default of about one second). The
  * waits run out, the kernel records FMLP_ERR_DEVICE_TIMEOUT and returns; the output is then

@@ -173,3 +173,26 @@ def test_one_launch_on_row_strided_views(fused):
     assert_parity(np.ascontiguousarray(out[:, ypad:ypad + D]),
                   oracle.mlp_gelu(x, W1, b1, W2, b2, gelu_mode=oracle.GELU_ERF), "strided")
     assert np.all(out[:, :ypad] == 0x7FBF) and np.all(out[:, ypad + D:] == 0x7FBF)
+
+
+def test_one_launch_grid_barrier_wait_runs_out_and_reports(fused):
+    """More CTAs than can be resident (whole clusters whose tiles lie past the last weight
+    row): the resident ones wait at the grid barrier for CTAs that cannot start until they
+    leave; the bounded wait runs out (2 ms), the status says where, and the counter heals
+    (every CTA still arrives once), so the next calls are correct."""
+    T, D, H = 16, 1024, 2048
+    ins = mlp_inputs(T, D, H, D)
+    assert fm.fmlp_device_status() == fm.FMLP_OK
+    fm.fmlp_test_decode_overload(3 * torch.cuda.get_device_properties(0).multi_processor_count,
+                                 2000)
+    try:
+        run_mlp(ins, T, D, H, D, fm.FMLP_GELU_TANH)
+    finally:
+        fm.fmlp_test_decode_overload(0, 0)
+    assert fm.fmlp_device_status() == fm.FMLP_ERR_DEVICE_TIMEOUT
+    assert "few-token block (grid barrier)" in fm.fmlp_last_error(), fm.fmlp_last_error()
+    assert fm.fmlp_device_status() == fm.FMLP_OK
+    ref = oracle.mlp_gelu(*ins, gelu_mode=oracle.GELU_TANH)
+    for _ in range(2):
+        assert_parity(run_mlp(ins, T, D, H, D, fm.FMLP_GELU_TANH), ref, "after a timeout")
+    assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()

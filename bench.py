@@ -544,6 +544,14 @@ def run_extras(fm, synth, torch, np, dev, stream, events_time, pk):
         # raw stream launches (no graph) too
         ms_stream = events_time(lambda: twenty(stream), 10) / 20
         entry["us_stream_launched"] = round(ms_stream * 1e3, 2)
+        entry["kernels"] = fm.fmlp_describe_plan("mlp", T, w.D, w.H, w.Dout)
+        if "one few-token tcgen05 launch" in entry["kernels"]:
+            # the same forwards as two few-token launches, which the plan does not choose here
+            fm.fmlp_test_fewtoken_block(-1)
+            try:
+                entry["us_two_launches"] = round(graph_time(torch, dev, twenty, 20) / 20 * 1e3, 2)
+            finally:
+                fm.fmlp_test_fewtoken_block(0)
         # oracle agreement of the last forward (weight set 4)
         one(stream, 4)
         torch.cuda.synchronize(dev)

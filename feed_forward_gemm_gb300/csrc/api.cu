@@ -2089,6 +2089,29 @@ fmlp_status fmlp_test_prefer_decode(int on) {
   return FMLP_OK;
 }
 
+fmlp_status fmlp_test_two_stage_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2,
+                                         int lists, int mc, uint16_t* start, uint16_t* item,
+                                         int64_t* n_items) {
+  t_last_error.clear();
+  if (!start || !item || !n_items) {
+    set_error("start, item and n_items must not be NULL");
+    return FMLP_ERR_NULL;
+  }
+  const int per1 = mc == 2 ? (num_n1 + 1) / 2 : num_n1;
+  const int groups = mc == 2 ? (num_m + 1) / 2 : num_m;
+  if (num_m < 1 || num_m > kTwoMaxBands || num_n1 < 1 || num_n2 < 1 || kb1 < 1 || kb2 < 1 ||
+      lists < 1 || lists > kTwoMaxPairs || (mc != 1 && mc != 2) ||
+      static_cast<int64_t>(num_m) * per1 + static_cast<int64_t>(groups) * num_n2 > kTwoMaxItems) {
+    set_error("schedule shape out of range");
+    return FMLP_ERR_SHAPE;
+  }
+  const TwoSchedule sc = two_schedule(num_m, num_n1, num_n2, kb1, kb2, lists, mc);
+  for (int i = 0; i <= lists; ++i) start[i] = sc.start[i];
+  for (size_t i = 0; i < sc.item.size(); ++i) item[i] = sc.item[i];
+  *n_items = static_cast<int64_t>(sc.item.size());
+  return FMLP_OK;
+}
+
 fmlp_status fmlp_test_fewtoken_block(int mode) {
   t_last_error.clear();
   if (mode < -1 || mode > 1) {

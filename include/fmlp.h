@@ -349,6 +349,18 @@ FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
  * FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_two_stage(int mode);
 
+/* The item lists of a two-stage launch (host only, no device needed), for checking the
+ * schedule: num_m bands of 256 rows, num_n1 first-stage and num_n2 down N tiles, kb1 and kb2
+ * K steps of 64 per tile, `lists` item lists of mc (1 or 2) CTA pairs each. First-stage items
+ * are u = band * per1 + j (per1 = num_n1, or (num_n1 + 1) / 2 when mc = 2); down items follow,
+ * n1 + group * num_n2 + n (a group is one band, or two bands when mc = 2). Writes
+ * start[0 .. lists] (list l runs item[start[l] .. start[l + 1])) and the items (at most 2048),
+ * and their count to *n_items. Shape out of range: FMLP_ERR_SHAPE; a NULL pointer:
+ * FMLP_ERR_NULL. */
+FMLP_API fmlp_status fmlp_test_two_stage_schedule(int num_m, int num_n1, int num_n2, int kb1,
+                                                  int kb2, int lists, int mc, uint16_t* start,
+                                                  uint16_t* item, int64_t* n_items);
+
 /* Plan switch for the few-token block launch, process-wide. Under FMLP_PLAN_TC a GeGLU block
  * of 2..64 tokens, or an MLP block of 2..128, can run both layers in ONE launch of the
  * few-token kernel's design (weights as the MMA's M side, K split over a cluster): layer 1 to

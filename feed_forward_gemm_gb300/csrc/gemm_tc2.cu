@@ -30,10 +30,12 @@
 // until every first-stage tile of that band has been stored: each epilogue warp, once the TMA
 // stores of its rows of a first-stage tile have completed, adds 1 to the band's counter with
 // release semantics; the producers of a down tile poll the counter with acquire semantics and
-// fence the async proxy before their TMA loads of the intermediate. The host zeroes the
-// counters before the launch. A pair's items only wait on items assigned before them, and
-// every pair is resident (the grid is at most the co-resident pairs), so the waits cannot
-// form a cycle.
+// fence the async proxy before their TMA loads of the intermediate. The counters are zero when
+// the module loads and the last CTA of each launch puts them back to zero. A pair's items only
+// wait on items assigned before them, and every pair is resident (the grid is at most the
+// co-resident pairs), so the waits cannot form a cycle. With MC = 2 two pairs of a 4-CTA
+// cluster run one list, each item one tile per pair, and share their loads of the common
+// operand (multicast).
 //
 // GROUPED (mixture of experts): as in the single-SM kernel, the rows of A are grouped by expert
 // with the E + 1 offsets read on the device, each group's tiles walk 256-row tile fastest, each CTA

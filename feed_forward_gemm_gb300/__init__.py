@@ -79,7 +79,7 @@ _SIGNATURES = {
     "fmlp_test_prefer_decode": (_INT, [_INT]),
     "fmlp_test_two_stage": (_INT, [_INT]),
     "fmlp_test_fewtoken_block": (_INT, [_INT]),
-    "fmlp_test_two_stage_schedule": (_INT, [_INT, _INT, _INT, _INT, _INT, _INT, _INT, _P, _P, _P]),
+    "fmlp_test_two_stage_schedule": (_INT, [_INT, _INT, _INT, _INT, _INT, _INT, _P, _P, _P]),
     "fmlp_test_inject": (_INT, [_INT, _I64, _I64]),
     "fmlp_status_string": (ctypes.c_char_p, [_INT]),
     "fmlp_last_error": (ctypes.c_char_p, []),
@@ -340,20 +340,18 @@ def fmlp_test_prefer_decode(on, raise_on_error=True):
 
 
 def fmlp_test_two_stage(mode, raise_on_error=True):
-    """Two-stage block launch: 0 automatic, 1 whenever accepted, 2 the same with two CTA pairs
-    per cluster sharing operand loads (multicast), -1 never (process-wide)."""
+    """Two-stage block launch: 0 automatic, 1 whenever accepted, -1 never (process-wide)."""
     st = load().fmlp_test_two_stage(int(mode))
     return _check(st, "fmlp_test_two_stage", raise_on_error)
 
 
-def fmlp_test_two_stage_schedule(num_m, num_n1, num_n2, kb1, kb2, lists, mc=1):
+def fmlp_test_two_stage_schedule(num_m, num_n1, num_n2, kb1, kb2, pairs):
     """The two-stage launch's item lists for a shape (host only): (start, items) as lists."""
-    start = (ctypes.c_uint16 * (int(lists) + 1))()
+    start = (ctypes.c_uint16 * (int(pairs) + 1))()
     item = (ctypes.c_uint16 * 2048)()
     n = ctypes.c_int64(0)
     st = load().fmlp_test_two_stage_schedule(int(num_m), int(num_n1), int(num_n2), int(kb1),
-                                             int(kb2), int(lists), int(mc), start, item,
-                                             ctypes.byref(n))
+                                             int(kb2), int(pairs), start, item, ctypes.byref(n))
     _check(st, "fmlp_test_two_stage_schedule", True)
     return list(start), list(item[:n.value])
 

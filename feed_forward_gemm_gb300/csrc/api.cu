@@ -51,7 +51,6 @@ struct DeviceState {
   int sms = 0;
   int major = 0, minor = 0;
   int max_pairs = 0;   // co-resident CTA pairs of the pair GEMM (0: pair kernel unavailable)
-  int max_quads = 0;   // co-resident 4-CTA clusters of the multicast two-stage kernel
   // co-resident clusters of 1, 2, 4, 8 few-token CTAs (0: unknown, assume sms / size)
   int skinny_clusters[4] = {0, 0, 0, 0};
   // co-resident clusters of 1, 2, 4, 8 CTAs of the few-token block kernel (0: unknown: the
@@ -143,10 +142,6 @@ fmlp_status device_state(DeviceState** out) {
     d.status = static_cast<int*>(p);
     if (gemm_tc2_max_pairs(&d.max_pairs) != cudaSuccess) {
       d.max_pairs = 0;
-      (void)cudaGetLastError();
-    }
-    if (gemm_tc2_max_quads(&d.max_quads) != cudaSuccess) {
-      d.max_quads = 0;
       (void)cudaGetLastError();
     }
     for (int i = 0; i < 4; ++i) {
@@ -792,97 +787,89 @@ constexpr int kTwoGroup = 8;
 constexpr int64_t kTwoMaxWeightBytes = 64ll << 20;
 
 struct TwoSchedule {
-  // the key: bands, first-stage N tiles, down N tiles, K steps of each stage, item lists, and
-  // pairs per list (mc = 2: two pairs run one list, each item one tile per pair)
-  int num_m = 0, num_n1 = 0, num_n2 = 0, kb1 = 0, kb2 = 0, lists = 0, mc = 0;
+  // the key: bands, first-stage N tiles, down N tiles, K steps of each stage, pairs
+  int num_m = 0, num_n1 = 0, num_n2 = 0, kb1 = 0, kb2 = 0, pairs = 0;
   std::vector<uint16_t> start, item;
-  double makespan = 0.0;     // estimated, in 64-deep K steps of one list
-  double two_launch = 0.0;   // the same estimate for two round-robin launches on as many pairs
+  double makespan = 0.0;     // estimated, in 64-deep K steps of one pair
+  double two_launch = 0.0;   // the same estimate for two round-robin launches
 };
 
-// List scheduling of the items over the lists (each list runs in order on its pair, or its two
-// pairs), in units of one 64-deep K step. The list that frees up first takes a down item whose
-// bands are complete while fewer than `early` down items have been placed ahead of the last
-// first-stage item, else the next first-stage item, else the down item
-// whose bands complete first (waiting for them). A down item is only placed once every
-// first-stage item of its bands has been, so every wait in the lists is on an item placed
-// earlier: with all pairs resident, the waits end. Returns the estimated makespan.
-// Items: first stage u = band * per1 + j (per1 = N tiles, or N tile pairs when mc = 2), taken
-// in groups of kTwoGroup bands with the band running fastest; then down items
-// n1 + group * num_n2 + n, a group being one band (or two when mc = 2).
+// List scheduling of the items over the pairs (each pair runs its list in order), in units
+// of one 64-deep K step. The pair that frees up first takes a down tile whose band is complete
+// while fewer than `early` down tiles have been placed ahead of the last first-stage tile, else
+// the next first-stage tile, else the down tile whose band completes first (waiting for it).
+// A down tile is only placed once every first-stage tile of its band has been, so every wait
+// in the lists is on an item placed earlier: with all pairs resident, the waits end. Returns
+// the estimated makespan. Items: first-stage u = band * num_n1 + j, taken in groups of
+// kTwoGroup bands with the band running fastest; then down items n1 + band * num_n2 + n.
 double list_schedule(const TwoSchedule& sc, int early, std::vector<std::vector<uint16_t>>* lists) {
-  const int num_m = sc.num_m, P = sc.lists, mc = sc.mc;
-  const int per1 = mc == 2 ? (sc.num_n1 + 1) / 2 : sc.num_n1;
-  const int groups = (num_m + mc - 1) / mc;
-  const int n1 = num_m * per1, n2 = groups * sc.num_n2;
+  const int num_m = sc.num_m, P = sc.pairs, per1 = sc.num_n1;
+  const int n1 = num_m * per1, n2 = num_m * sc.num_n2;
   const double c1 = sc.kb1 + kTwoTileOverhead, c2 = sc.kb2 + kTwoTileOverhead;
   lists->assign(P, {});
-  std::vector<double> free_at(P, 0.0), group_ready(groups, 0.0);
-  std::vector<int> band_left(num_m, per1), group_left(groups, 0);
-  for (int b = 0; b < num_m; ++b) ++group_left[b / mc];
-  std::vector<int> pending;   // down items of complete groups, not yet placed
+  std::vector<double> free_at(P, 0.0), band_ready(num_m, 0.0);
+  std::vector<int> band_left(num_m, per1);
+  std::vector<int> pending;   // down items of complete bands, not yet placed
   int next1 = 0, taken_early = 0;
-  auto group_of = [&](int t) { return (t - n1) / sc.num_n2; };
+  auto band_of = [&](int t) { return (t - n1) / sc.num_n2; };
   for (int placed = 0; placed < n1 + n2; ++placed) {
     int p = 0;
     for (int q = 1; q < P; ++q)
       if (free_at[q] < free_at[p]) p = q;
     int best = -1;
     for (int i = 0; i < static_cast<int>(pending.size()); ++i)
-      if (best < 0 || group_ready[group_of(pending[i])] < group_ready[group_of(pending[best])])
+      if (best < 0 || band_ready[band_of(pending[i])] < band_ready[band_of(pending[best])])
         best = i;
     const bool down_now =
-        best >= 0 && taken_early < early && group_ready[group_of(pending[best])] <= free_at[p];
+        best >= 0 && taken_early < early && band_ready[band_of(pending[best])] <= free_at[p];
     if (!down_now && next1 < n1) {
       // first-stage items in groups of kTwoGroup bands, the band running fastest, so the
       // pairs in flight read each weight tile at about the same time from L2
       const int k = next1++, per_group = kTwoGroup * per1, kg = k / per_group;
       const int r = k - kg * per_group, gb = std::min(kTwoGroup, num_m - kg * kTwoGroup);
       const int t = (kg * kTwoGroup + r % gb) * per1 + r / gb;
-      const int b = t / per1, g = b / mc;
+      const int b = t / per1;
       (*lists)[p].push_back(static_cast<uint16_t>(t));
       free_at[p] += c1;
-      group_ready[g] = std::max(group_ready[g], free_at[p]);
-      if (--band_left[b] == 0 && --group_left[g] == 0)
-        for (int j = 0; j < sc.num_n2; ++j) pending.push_back(n1 + g * sc.num_n2 + j);
+      band_ready[b] = std::max(band_ready[b], free_at[p]);
+      if (--band_left[b] == 0)
+        for (int j = 0; j < sc.num_n2; ++j) pending.push_back(n1 + b * sc.num_n2 + j);
     } else {
       if (next1 < n1) ++taken_early;
       const int t = pending[best];
       pending.erase(pending.begin() + best);
       (*lists)[p].push_back(static_cast<uint16_t>(t));
-      free_at[p] = std::max(free_at[p], group_ready[group_of(t)]) + c2;
+      free_at[p] = std::max(free_at[p], band_ready[band_of(t)]) + c2;
     }
   }
   return *std::max_element(free_at.begin(), free_at.end());
 }
 
-// The schedule with the shortest estimated makespan over a sweep of `early` (the down items
+// The schedule with the shortest estimated makespan over a sweep of `early` (the down tiles
 // that do not fill whole waves at the end are the ones worth running early).
 void build_two_schedule(TwoSchedule* sc) {
-  const int groups = (sc->num_m + sc->mc - 1) / sc->mc;
-  const int n2 = groups * sc->num_n2;
+  const int n2 = sc->num_m * sc->num_n2;
   std::vector<std::vector<uint16_t>> lists, best_lists;
   double best = -1.0;
   const int step = std::max(1, n2 / 16);
   for (int e = -1; e <= n2; e += (e < 0 ? 1 : step)) {
-    const int early = e < 0 ? n2 % sc->lists : e;
+    const int early = e < 0 ? n2 % sc->pairs : e;
     const double ms = list_schedule(*sc, early, &lists);
     if (best < 0.0 || ms < best) {
       best = ms;
       best_lists.swap(lists);
     }
   }
-  sc->start.assign(sc->lists + 1, 0);
+  sc->start.assign(sc->pairs + 1, 0);
   sc->item.clear();
-  for (int p = 0; p < sc->lists; ++p) {
+  for (int p = 0; p < sc->pairs; ++p) {
     sc->item.insert(sc->item.end(), best_lists[p].begin(), best_lists[p].end());
     sc->start[p + 1] = static_cast<uint16_t>(sc->item.size());
   }
   sc->makespan = best;
   // the same tiles as two round-robin launches over as many pairs, for the automatic choice
-  const int pairs = sc->lists * sc->mc;
-  const int t1 = sc->num_m * sc->num_n1, t2 = sc->num_m * sc->num_n2;
-  const double waves1 = (t1 + pairs - 1) / pairs, waves2 = (t2 + pairs - 1) / pairs;
+  const int n1 = sc->num_m * sc->num_n1;
+  const double waves1 = (n1 + sc->pairs - 1) / sc->pairs, waves2 = (n2 + sc->pairs - 1) / sc->pairs;
   sc->two_launch = waves1 * (sc->kb1 + kTwoTileOverhead) + waves2 * (sc->kb2 + kTwoTileOverhead);
 }
 
@@ -893,12 +880,11 @@ TwoSchedule g_two_cache[kTwoCache];
 int g_two_next = 0;
 
 // A copy: the cached entry may be replaced by another thread once the lock is released.
-TwoSchedule two_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2, int lists,
-                         int mc) {
+TwoSchedule two_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2, int pairs) {
   std::lock_guard<std::mutex> lock(g_two_mu);
   for (const TwoSchedule& c : g_two_cache)
-    if (c.lists == lists && c.mc == mc && c.num_m == num_m && c.num_n1 == num_n1 &&
-        c.num_n2 == num_n2 && c.kb1 == kb1 && c.kb2 == kb2)
+    if (c.pairs == pairs && c.num_m == num_m && c.num_n1 == num_n1 && c.num_n2 == num_n2 &&
+        c.kb1 == kb1 && c.kb2 == kb2)
       return c;
   TwoSchedule& c = g_two_cache[g_two_next];
   g_two_next = (g_two_next + 1) % kTwoCache;
@@ -907,20 +893,17 @@ TwoSchedule two_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2, in
   c.num_n2 = num_n2;
   c.kb1 = kb1;
   c.kb2 = kb2;
-  c.lists = lists;
-  c.mc = mc;
+  c.pairs = pairs;
   build_two_schedule(&c);
   return c;
 }
 
-// Test hook (fmlp_test_two_stage): 0 automatic, -1 never, 1 whenever the shape is accepted,
-// 2 the same with two pairs per cluster sharing their operand loads (multicast).
+// Test hook (fmlp_test_two_stage): 0 automatic, -1 never, 1 whenever the shape is accepted.
 std::atomic<int> g_two_stage{0};
 
-// A two-stage launch of this block (lists item lists of mc pairs each), or lists = 0 when it
-// does not take one.
+// Pairs of a two-stage launch of this block, or 0 when it does not take one.
 struct TwoPlan {
-  int lists = 0, mc = 1;
+  int pairs = 0;
   int num_m = 0, num_n1 = 0, num_n2 = 0, kb1 = 0, kb2 = 0;
 };
 
@@ -939,20 +922,16 @@ TwoPlan plan_two(const DeviceState& d, int epi1, int64_t T, int64_t D, int64_t H
   if (w_bytes > kTwoMaxWeightBytes || num_m > kTwoMaxBands || items > kTwoMaxItems) return tp;
   if (mode == 0 && !(choose_gemm(d, epi1, T, H).pair && choose_gemm(d, EPI_BIAS, T, Dout).pair))
     return tp;
-  const int mc = mode == 2 ? 2 : 1;
-  if (mc == 2 && d.max_quads < 1) return tp;
-  const int lists = std::min(std::min(mc == 2 ? d.max_quads : d.max_pairs, kTwoMaxPairs),
-                             static_cast<int>(items));
+  const int pairs = std::min(std::min(d.max_pairs, kTwoMaxPairs), static_cast<int>(items));
   const int kb1 = static_cast<int>((D + 63) / 64), kb2 = static_cast<int>((H + 63) / 64);
   if (mode == 0) {
     // only where the list schedule is estimated clearly shorter than two launches (at 0.92
     // of their estimate a 8192x1024x4096 GeGLU block measured 2.6 % slower in one launch)
     const TwoSchedule sc = two_schedule(static_cast<int>(num_m), static_cast<int>(num_n1),
-                                        static_cast<int>(num_n2), kb1, kb2, lists, mc);
+                                        static_cast<int>(num_n2), kb1, kb2, pairs);
     if (sc.makespan > 0.9 * sc.two_launch) return tp;
   }
-  tp.lists = lists;
-  tp.mc = mc;
+  tp.pairs = pairs;
   tp.num_m = static_cast<int>(num_m);
   tp.num_n1 = static_cast<int>(num_n1);
   tp.num_n2 = static_cast<int>(num_n2);
@@ -969,15 +948,14 @@ fmlp_status launch_two(DeviceState& d, int epi1, const void* x, const void* W1a,
                        cudaStream_t s, int64_t ldx, int64_t ldy, bool* ran) {
   *ran = false;
   const TwoPlan tp = plan_two(d, epi1, T, D, H, Dout);
-  if (tp.lists < 1) return FMLP_OK;
+  if (tp.pairs < 1) return FMLP_OK;
   const int slot = stream_slot(d, s);
   if (slot < 0) return FMLP_OK;
   FMLP_LAUNCH_GUARD("two-stage launch");
   // test hook: a band count one above what the first stage adds, so every down tile's wait
   // runs out
   const bool starve = take_injection(g_inject_skip);
-  const TwoSchedule sc =
-      two_schedule(tp.num_m, tp.num_n1, tp.num_n2, tp.kb1, tp.kb2, tp.lists, tp.mc);
+  const TwoSchedule sc = two_schedule(tp.num_m, tp.num_n1, tp.num_n2, tp.kb1, tp.kb2, tp.pairs);
   const bool geglu = epi1 == EPI_GEGLU;
   GemmLaunch L;
   memset(&L, 0, sizeof L);
@@ -1004,14 +982,9 @@ fmlp_status launch_two(DeviceState& d, int epi1, const void* x, const void* W1a,
     const unsigned long long tmo = g_inject_timeout_ns.load(std::memory_order_relaxed);
     if (tmo) L.timeout_ns = tmo;
   }
-  L.grid = 2 * tp.mc * tp.lists;
+  L.grid = 2 * tp.pairs;
   TwoStageLaunch T2;
   memset(&T2, 0, sizeof T2);
-  T2.mc = tp.mc;
-  if (tp.mc == 2) {
-    FMLP_TRY(make_map(&T2.tmAh, x, T, D, 64, "x", ldx));
-    FMLP_TRY(make_map(&T2.tmB2h, W2, Dout, H, 64, geglu ? "Wd" : "W2"));
-  }
   FMLP_TRY(make_map(&T2.tmA2, h, T, H, 128, "intermediate"));
   FMLP_TRY(make_map(&T2.tmB2, W2, Dout, H, 128, geglu ? "Wd" : "W2"));
   FMLP_TRY(make_map(&T2.tmY2, y, T, Dout, 32, "y", ldy));
@@ -1020,7 +993,7 @@ fmlp_status launch_two(DeviceState& d, int epi1, const void* x, const void* W1a,
   T2.band_extra = starve ? 1 : 0;
   T2.N2 = static_cast<int>(Dout);
   T2.K2 = static_cast<int>(H);
-  T2.n1 = tp.num_m * (tp.mc == 2 ? (tp.num_n1 + 1) / 2 : tp.num_n1);
+  T2.n1 = tp.num_m * tp.num_n1;
   T2.n_items = static_cast<int>(sc.item.size());
   T2.start = sc.start.data();
   T2.item = sc.item.data();
@@ -1897,12 +1870,11 @@ static std::string describe_two(const TwoPlan& tp, const char* name1, int64_t T,
   char b[384];
   snprintf(b, sizeof b,
            "%s and down: one tcgen05 CTA-pair launch for both layers, %d first-stage and %d "
-           "down 256-row tiles listed over %d pairs%s (each band's down tiles after its "
+           "down 256-row tiles listed over %d pairs (each band's down tiles after its "
            "first-stage tiles), T=%lld D=%lld H=%lld Dout=%lld, grid=%d",
-           name1, tp.num_m * tp.num_n1, tp.num_m * tp.num_n2, tp.mc * tp.lists,
-           tp.mc == 2 ? " in clusters of two sharing operand loads (multicast)" : "",
+           name1, tp.num_m * tp.num_n1, tp.num_m * tp.num_n2, tp.pairs,
            static_cast<long long>(T), static_cast<long long>(D), static_cast<long long>(H),
-           static_cast<long long>(Dout), 2 * tp.mc * tp.lists);
+           static_cast<long long>(Dout), 2 * tp.pairs);
   return b;
 }
 
@@ -1949,7 +1921,7 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += describe_gemv(*d, "gate/up", T, D, H, 2) + "; " + describe_gemv(*d, "down", T, H, D);
     } else if (const FewBlockPlan fp = plan_fewblock(*d, EPI_GEGLU, T, D, H, D); fp.ok) {
       r += describe_fewblock(fp, "gate/up", T, D, H, D);
-    } else if (const TwoPlan tp = plan_two(*d, EPI_GEGLU, T, D, H, D); tp.lists > 0) {
+    } else if (const TwoPlan tp = plan_two(*d, EPI_GEGLU, T, D, H, D); tp.pairs > 0) {
       r += describe_two(tp, "gate/up", T, D, H, D);
     } else {
       r += describe_gemm(*d, "gate/up", EPI_GEGLU, T, H, D) + "; " +
@@ -1968,7 +1940,7 @@ fmlp_status fmlp_describe_plan(int op, int64_t T, int64_t D, int64_t H, int64_t 
       r += describe_gemv(*d, "up", T, D, H) + "; " + describe_gemv(*d, "down", T, H, Dout);
     else if (const FewBlockPlan fp = plan_fewblock(*d, EPI_BIAS_GELU, T, D, H, Dout); fp.ok)
       r += describe_fewblock(fp, "up", T, D, H, Dout);
-    else if (const TwoPlan tp = plan_two(*d, EPI_BIAS_GELU, T, D, H, Dout); tp.lists > 0)
+    else if (const TwoPlan tp = plan_two(*d, EPI_BIAS_GELU, T, D, H, Dout); tp.pairs > 0)
       r += describe_two(tp, "up", T, D, H, Dout);
     else
       r += describe_gemm(*d, "up", EPI_BIAS_GELU, T, H, D) + "; " +
@@ -2090,23 +2062,21 @@ fmlp_status fmlp_test_prefer_decode(int on) {
 }
 
 fmlp_status fmlp_test_two_stage_schedule(int num_m, int num_n1, int num_n2, int kb1, int kb2,
-                                         int lists, int mc, uint16_t* start, uint16_t* item,
+                                         int pairs, uint16_t* start, uint16_t* item,
                                          int64_t* n_items) {
   t_last_error.clear();
   if (!start || !item || !n_items) {
     set_error("start, item and n_items must not be NULL");
     return FMLP_ERR_NULL;
   }
-  const int per1 = mc == 2 ? (num_n1 + 1) / 2 : num_n1;
-  const int groups = mc == 2 ? (num_m + 1) / 2 : num_m;
   if (num_m < 1 || num_m > kTwoMaxBands || num_n1 < 1 || num_n2 < 1 || kb1 < 1 || kb2 < 1 ||
-      lists < 1 || lists > kTwoMaxPairs || (mc != 1 && mc != 2) ||
-      static_cast<int64_t>(num_m) * per1 + static_cast<int64_t>(groups) * num_n2 > kTwoMaxItems) {
+      pairs < 1 || pairs > kTwoMaxPairs ||
+      static_cast<int64_t>(num_m) * (num_n1 + num_n2) > kTwoMaxItems) {
     set_error("schedule shape out of range");
     return FMLP_ERR_SHAPE;
   }
-  const TwoSchedule sc = two_schedule(num_m, num_n1, num_n2, kb1, kb2, lists, mc);
-  for (int i = 0; i <= lists; ++i) start[i] = sc.start[i];
+  const TwoSchedule sc = two_schedule(num_m, num_n1, num_n2, kb1, kb2, pairs);
+  for (int i = 0; i <= pairs; ++i) start[i] = sc.start[i];
   for (size_t i = 0; i < sc.item.size(); ++i) item[i] = sc.item[i];
   *n_items = static_cast<int64_t>(sc.item.size());
   return FMLP_OK;
@@ -2124,8 +2094,8 @@ fmlp_status fmlp_test_fewtoken_block(int mode) {
 
 fmlp_status fmlp_test_two_stage(int mode) {
   t_last_error.clear();
-  if (mode < -1 || mode > 2) {
-    set_error("mode = %d, expected -1, 0, 1 or 2", mode);
+  if (mode < -1 || mode > 1) {
+    set_error("mode = %d, expected -1, 0 or 1", mode);
     return FMLP_ERR_SHAPE;
   }
   g_two_stage.store(mode, std::memory_order_relaxed);

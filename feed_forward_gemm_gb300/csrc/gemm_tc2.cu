@@ -33,9 +33,7 @@
 // fence the async proxy before their TMA loads of the intermediate. The counters are zero when
 // the module loads and the last CTA of each launch puts them back to zero. A pair's items only
 // wait on items assigned before them, and every pair is resident (the grid is at most the
-// co-resident pairs), so the waits cannot form a cycle. With MC = 2 two pairs of a 4-CTA
-// cluster run one list, each item one tile per pair, and share their loads of the common
-// operand (multicast).
+// co-resident pairs), so the waits cannot form a cycle.
 //
 // GROUPED (mixture of experts): as in the single-SM kernel, the rows of A are grouped by expert
 // with the E + 1 offsets read on the device, each group's tiles walk 256-row tile fastest, each CTA
@@ -125,8 +123,6 @@ struct TwoArgs<true> {
   CUtensorMap tmA2;                   // second-stage A: the intermediate [M, K2], 128-row box
   CUtensorMap tmB2;                   // second-stage weights [N2, K2], 128-row box
   CUtensorMap tmY2;                   // output [M, N2], 32-row box
-  CUtensorMap tmAh;                   // MC = 2: first-stage A (x), 64-row box
-  CUtensorMap tmB2h;                  // MC = 2: second-stage weights, 64-row box
   const __nv_bfloat16* bias2;         // [N2] or nullptr
   unsigned int* band;                 // [num_m] counters, zero at launch
   int N2, K2, n1, band_target;        // n1: first-stage items; target: 8 x first-stage N tiles
@@ -140,25 +136,13 @@ __device__ __forceinline__ int two_n1(const TwoArgs<false>&) { return 1 << 30; }
 // Item t of a two-stage list -> stage, 256-row band, N tile. First-stage items are numbered
 // band-major (t = band * num_n1 + n tile; the host orders them), second-stage items follow
 // (n1 + band * num_n2 + n tile).
-// MC = 2 (two pairs per cluster, q = 0 or 1 the pair's place in it): an item is one tile per
-// pair. A first-stage item (band, j) gives pair q the N tile 2j + q (the pairs share the band
-// of x); a second-stage item (g, n) gives pair q band 2g + q, N tile n (they share the weight
-// rows). A tile past the last N tile or band is computed on zero-filled operands and its
-// stores are clipped.
-template <int MC>
-__device__ __forceinline__ void two_tile(int t, int n1, int num_n1, int num_n2, int q,
-                                         bool& second, int& tm, int& tn) {
+__device__ __forceinline__ void two_tile(int t, int n1, int num_n1, int num_n2, bool& second,
+                                         int& tm, int& tn) {
   second = t >= n1;
   const int u = second ? t - n1 : t;
-  const int per = second ? num_n2 : (MC == 2 ? (num_n1 + 1) / 2 : num_n1);
+  const int per = second ? num_n2 : num_n1;
   tm = u / per;
   tn = u - tm * per;
-  if (MC == 2) {
-    if (second)
-      tm = 2 * tm + q;
-    else
-      tn = 2 * tn + q;
-  }
 }
 
 // Band counters of the two-stage launches, one row of kTwoBandRow words per stream slot (the
@@ -168,10 +152,8 @@ constexpr int kTwoBandRow = 128;
 static_assert(kTwoMaxBands < kTwoBandRow, "band row holds the bands and the finished count");
 __device__ unsigned int g_two_band[kDecodeSlots * kTwoBandRow];
 
-// MC: CTA pairs per cluster (2 only with TWO: the pairs of a cluster run one item list, and
-// each pair loads half of the operand they share, multicast to both).
-template <int BN, int EPI, bool GROUPED, bool TWO, int MC = 1>
-__global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1)
+template <int BN, int EPI, bool GROUPED, bool TWO>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1,
@@ -180,7 +162,6 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
                     int gelu_mode, int group, int* status, uint64_t timeout_ns,
                     const int* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ ydir,
                     int ldy, int skip_first_load, const __grid_constant__ TwoArgs<TWO> two) {
-  static_assert(MC == 1 || (MC == 2 && TWO && !GROUPED), "multicast pairs: two-stage lists");
   using C = PairCfg<BN>;
   constexpr int kPairStages = C::STAGES;
   constexpr int kPairStage = C::STAGE;
@@ -198,13 +179,9 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;          // in the pair: 0 issues the MMAs, 1 is its peer
-  const uint32_t q = crank >> 1;             // the pair's place in its cluster (MC = 2)
-  const uint32_t lead = crank & ~1u;         // this pair's even CTA
+  const uint32_t rank = cluster_ctarank();   // 0: issues the MMAs, 1: its peer
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  const int list = MC == 2 ? static_cast<int>(blockIdx.x >> 2) : pair;   // TWO: item list
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -213,7 +190,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
     prefetch_tmap(&tmY);
     for (int s = 0; s < kPairStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC);   // released by the MMAs of every pair that reads the slot
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -262,11 +239,11 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
   // This pair's items: t = pair, pair + npairs, ... below num_tiles, or (TWO) its list.
   int n_items = 0;
   if constexpr (TWO)
-    n_items = two.start[list + 1] - two.start[list];
+    n_items = two.start[pair + 1] - two.start[pair];
   else
     n_items = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
   auto item_at = [&](int k) -> int {
-    if constexpr (TWO) return two.item[two.start[list] + k];
+    if constexpr (TWO) return two.item[two.start[pair] + k];
     return pair + k * npairs;
   };
   // second-stage geometry (TWO)
@@ -279,9 +256,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint32_t full0 = mapa_shared(smem_u32(full), lead);   // even CTA's full[0]
-      // MC = 2: this CTA and its counterpart in the other pair receive the shared half-boxes
-      const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // even CTA's full[0]
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_phase_mask = 0;
@@ -293,7 +268,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
         if constexpr (GROUPED) {
           pair_group_tile(t, s_off, s_tp, ge, grow, grows, tn);
         } else if (TWO) {
-          two_tile<MC>(t, two_n1(two), num_n, num_n2, static_cast<int>(q), second, tm, tn);
+          two_tile(t, two_n1(two), num_n, num_n2, second, tm, tn);
         } else {
           pair_tile_coords(t, num_m, num_n, group, tm, tn);
         }
@@ -306,8 +281,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
           if (second) {
             // the band of the intermediate this down tile reads must be stored completely
             const uint64_t t0 = globaltimer_ns();
-            while (tm < num_m &&
-                   ld_acquire_u32(two.band + tm) < static_cast<unsigned>(two.band_target)) {
+            while (ld_acquire_u32(two.band + tm) < static_cast<unsigned>(two.band_target)) {
               if (globaltimer_ns() - t0 > timeout_ns) {
                 atomicCAS(status, 0, (SITE_BAND << 8) | kDeviceTimeoutCode);
                 ok = false;
@@ -348,25 +322,11 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
             continue;
           }
           const uint32_t fb = full0 + static_cast<uint32_t>(stage * 8);
-          if constexpr (MC == 2) {
-            // the shared operand in two 64-row halves, one per pair, each multicast to both
-            const int qo = static_cast<int>(q) * 64;
-            if (second) {
-              tma_load_2d_pair(sA, amap, fb, kb * kPairBK, a_row);
-              tma_load_2d_pair_mc(sB + qo * 128, &two.tmB2h, fb, kb * kPairBK, b_row + qo,
-                                  mc_mask);
-            } else {
-              tma_load_2d_pair_mc(sA + qo * 128, &two.tmAh, fb, kb * kPairBK, a_row + qo,
-                                  mc_mask);
-              tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
-            }
-          } else {
-            tma_load_2d_pair(sA, amap, fb, kb * kPairBK, a_row);
-            if constexpr (GROUPED)
-              tma_load_3d_pair(sB, bmap, fb, kb * kPairBK, b_row, ge);
-            else
-              tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
-          }
+          tma_load_2d_pair(sA, amap, fb, kb * kPairBK, a_row);
+          if constexpr (GROUPED)
+            tma_load_3d_pair(sB, bmap, fb, kb * kPairBK, b_row, ge);
+          else
+            tma_load_2d_pair(sB, bmap, fb, kb * kPairBK, b_row);
           issued_mask |= 1u << stage;
           last_phase_mask = (last_phase_mask & ~(1u << stage)) | (phase << stage);
           if (++stage == kPairStages) {
@@ -410,15 +370,14 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
           for (int kk = 0; kk < kPairBK / 16; ++kk)
             tc_mma_bf16_pair(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
                              (kb | kk) != 0 ? 1u : 0u);
-          // the slot is free again in every CTA whose loads fill it (MC = 2: all four)
-          tc_commit_pair_mc(&empty[stage], MC == 2 ? 0xF : 0x3);
+          tc_commit_pair_mc(&empty[stage], 0x3);
           if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(&tfull[buf], static_cast<uint16_t>(0x3u << lead));
+        tc_commit_pair_mc(&tfull[buf], 0x3);
       }
       tc_commit_pair(drain);
       mbar_wait(drain, 0, status, SITE_DRAIN, timeout_ns);
@@ -428,7 +387,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int wq = warp & 3;
     uint8_t* stg = stg_all + (warp - 2) * kStgPerWarp * kStgBytes;
-    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), lead);
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
     int sb = 0;
     int it = 0;
     for (int k = 0; k < n_items; ++k, ++it) {
@@ -438,7 +397,7 @@ __global__ void __cluster_dims__(2 * MC, 1, 1) __launch_bounds__(kPairThreads, 1
       if constexpr (GROUPED) {
         pair_group_tile(t, s_off, s_tp, ge, grow, grows, tn);
       } else if (TWO) {
-        two_tile<MC>(t, two_n1(two), num_n, num_n2, static_cast<int>(q), second, tm, tn);
+        two_tile(t, two_n1(two), num_n, num_n2, second, tm, tn);
       } else {
         pair_tile_coords(t, num_m, num_n, group, tm, tn);
       }
@@ -516,10 +475,10 @@ int gemm_tc2_group(int K) {
   return group < 2 ? 2 : (group > 16 ? 16 : group);
 }
 
-template <int BN, int EPI, bool GROUPED = false, bool TWO = false, int MC = 1>
+template <int BN, int EPI, bool GROUPED = false, bool TWO = false>
 static cudaError_t launch_pair(const GemmLaunch& L, const TwoArgs<TWO>& two) {
   using C = PairCfg<BN>;
-  auto kern = gemm_tc2_kernel<BN, EPI, GROUPED, TWO, MC>;
+  auto kern = gemm_tc2_kernel<BN, EPI, GROUPED, TWO>;
   static SmemAttrCache cache;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM, cache);
   if (e != cudaSuccess) return e;
@@ -554,12 +513,10 @@ cudaError_t gemm_tc2_launch(const GemmLaunch& L) {
 
 cudaError_t gemm_tc2_two_launch(const GemmLaunch& L, const TwoStageLaunch& T2) {
   const int pairs = L.grid / 2;
-  const int lists = pairs / (T2.mc == 2 ? 2 : 1);
   const int num_m = (L.M + 255) / 256;
-  if (L.grid < 2 || L.grid % (2 * T2.mc) != 0 || (T2.mc != 1 && T2.mc != 2) || L.bn != 256 ||
-      lists > kTwoMaxPairs || num_m > kTwoMaxBands || T2.n_items > kTwoMaxItems ||
-      T2.n_items < T2.n1 || !T2.start || !T2.item || T2.slot < 0 || T2.slot >= kDecodeSlots ||
-      (L.epi != EPI_GEGLU && L.epi != EPI_BIAS_GELU))
+  if (L.grid < 2 || (L.grid & 1) || L.bn != 256 || pairs > kTwoMaxPairs || num_m > kTwoMaxBands ||
+      T2.n_items > kTwoMaxItems || T2.n_items < T2.n1 || !T2.start || !T2.item ||
+      T2.slot < 0 || T2.slot >= kDecodeSlots || (L.epi != EPI_GEGLU && L.epi != EPI_BIAS_GELU))
     return cudaErrorInvalidValue;
   unsigned int* band = nullptr;
   cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&band), g_two_band);
@@ -569,24 +526,16 @@ cudaError_t gemm_tc2_two_launch(const GemmLaunch& L, const TwoStageLaunch& T2) {
   a.tmA2 = T2.tmA2;
   a.tmB2 = T2.tmB2;
   a.tmY2 = T2.tmY2;
-  a.tmAh = T2.tmAh;
-  a.tmB2h = T2.tmB2h;
   a.bias2 = static_cast<const __nv_bfloat16*>(T2.bias2);
   a.band = band + static_cast<size_t>(T2.slot) * kTwoBandRow;
   a.N2 = T2.N2;
   a.K2 = T2.K2;
   a.n1 = T2.n1;
-  // each first-stage tile adds one per epilogue warp of the pair to its band (MC = 2: the
-  // tiles of both pairs, one of them past the last N tile when the count is odd)
+  // each first-stage tile adds one per epilogue warp of the pair to its band
   const int bn_out = L.epi == EPI_GEGLU ? 128 : 256;
-  const int num_n1 = (L.N_out + bn_out - 1) / bn_out;
-  const int tiles_per_band = T2.mc == 2 ? 2 * ((num_n1 + 1) / 2) : num_n1;
-  a.band_target = 2 * kEpiWarps * tiles_per_band + T2.band_extra;
-  for (int p = 0; p <= lists; ++p) a.start[p] = T2.start[p];
+  a.band_target = 2 * kEpiWarps * ((L.N_out + bn_out - 1) / bn_out) + T2.band_extra;
+  for (int p = 0; p <= pairs; ++p) a.start[p] = T2.start[p];
   for (int i = 0; i < T2.n_items; ++i) a.item[i] = T2.item[i];
-  if (T2.mc == 2)
-    return L.epi == EPI_GEGLU ? launch_pair<256, EPI_GEGLU, false, true, 2>(L, a)
-                              : launch_pair<256, EPI_BIAS_GELU, false, true, 2>(L, a);
   return L.epi == EPI_GEGLU ? launch_pair<256, EPI_GEGLU, false, true>(L, a)
                             : launch_pair<256, EPI_BIAS_GELU, false, true>(L, a);
 }
@@ -616,22 +565,6 @@ cudaError_t gemm_tc2_max_pairs(int* pairs) {
   e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
   if (e != cudaSuccess) return e;
   *pairs = n;
-  return cudaSuccess;
-}
-
-cudaError_t gemm_tc2_max_quads(int* clusters) {
-  auto kern = gemm_tc2_kernel<256, EPI_GEGLU, false, true, 2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PairCfg<256>::SMEM);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<256>::SMEM;
-  int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-  if (e != cudaSuccess) return e;
-  *clusters = n;
   return cudaSuccess;
 }
 

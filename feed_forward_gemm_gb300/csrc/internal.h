@@ -78,20 +78,15 @@ struct TwoStageLaunch {
   CUtensorMap tmB2;   // second-stage weights [N2, K2], box {64, 128}
   CUtensorMap tmY2;   // output [M, N2], box {64, 32}
   const void* bias2;  // [N2] or nullptr
-  CUtensorMap tmAh;   // mc = 2: x with a 64-row box (each pair loads half of the shared band)
-  CUtensorMap tmB2h;  // mc = 2: second-stage weights with a 64-row box
-  int mc;             // CTA pairs per cluster and item list: 1, or 2 (shared operand multicast)
   int slot;           // band-counter row (per stream; launches in one row must not overlap)
   int band_extra;     // test hook: added to the complete band count (1: never reached)
   int N2, K2;
   int n_items;        // items in `item` (first-stage tiles + second-stage tiles)
   int n1;             // first-stage tiles (band-major numbering), second-stage ones follow
-  const uint16_t* start;   // [lists + 1]: list l runs item[start[l] .. start[l + 1])
+  const uint16_t* start;   // [pairs + 1]: pair p runs item[start[p] .. start[p + 1])
   const uint16_t* item;    // [n_items]
 };
 cudaError_t gemm_tc2_two_launch(const GemmLaunch& L, const TwoStageLaunch& T2);
-// Co-resident 4-CTA clusters of the two-stage kernel with two pairs per cluster.
-cudaError_t gemm_tc2_max_quads(int* clusters);
 
 // Few-token tcgen05 GEMM (weights as the MMA's M side, K split over a cluster; gemm_skinny.cu).
 constexpr int kSkinnyMaxT = 128;

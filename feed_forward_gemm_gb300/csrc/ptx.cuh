@@ -380,20 +380,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// tma_load_2d_pair with cluster multicast: the box lands at the same shared-memory offset in
-// every CTA of `mask`, and each destination's bytes are counted on the mbarrier at this
-// barrier's offset in the even CTA of the destination's own pair (the barrier address passed
-// is an even CTA's).
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* m,
-                                                    uint32_t bar_cluster_addr, int32_t c0,
-                                                    int32_t c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
 // 3-D variant of tma_load_2d_pair.
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m,
                                                  uint32_t bar_cluster_addr, int32_t c0,

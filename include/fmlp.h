@@ -336,29 +336,25 @@ FMLP_API fmlp_status fmlp_test_prefer_decode(int on);
  * the first layer's 256-row tiles and the down tiles share one list per pair, a down tile
  * waiting (bounded) until every first-layer tile of its 256 rows has been stored. mode 0 (the
  * default) takes it when both layers would run on the CTA-pair kernel anyway; mode 1 takes it
- * for every block it accepts (also the FMLP_TILES_PAIR policy's); mode 2 the same with two CTA
- * pairs per 4-CTA cluster running one item list, each pair loading half of the operand the two
- * share (the x band of a first-layer tile pair, the weight rows of a down tile pair) and
- * multicasting it to both; mode -1 never (two launches). The results are bit-identical either way: the same tiles, the same K order, the
+ * for every block it accepts (also the FMLP_TILES_PAIR policy's); mode -1 never (two
+ * launches). The results are bit-identical either way: the same tiles, the same K order, the
  * same roundings. The launch keeps one row of counters per stream, like FMLP_PLAN_DECODE, and
  * expects every one of its CTA pairs to be resident at once (a concurrent kernel on another
  * stream that holds SMs until this launch ends makes its waits run out with
  * FMLP_ERR_DEVICE_TIMEOUT). Under FMLP_INJECT_SKIP_LOAD, a two-stage launch takes the
  * injection instead as a band count that is never reached, so its down tiles' waits run out.
- * Switch it only while no other thread queries plans or launches. mode not in {-1, 0, 1, 2}:
+ * Switch it only while no other thread queries plans or launches. mode not in {-1, 0, 1}:
  * FMLP_ERR_SHAPE. */
 FMLP_API fmlp_status fmlp_test_two_stage(int mode);
 
 /* The item lists of a two-stage launch (host only, no device needed), for checking the
  * schedule: num_m bands of 256 rows, num_n1 first-stage and num_n2 down N tiles, kb1 and kb2
- * K steps of 64 per tile, `lists` item lists of mc (1 or 2) CTA pairs each. First-stage items
- * are u = band * per1 + j (per1 = num_n1, or (num_n1 + 1) / 2 when mc = 2); down items follow,
- * n1 + group * num_n2 + n (a group is one band, or two bands when mc = 2). Writes
- * start[0 .. lists] (list l runs item[start[l] .. start[l + 1])) and the items (at most 2048),
- * and their count to *n_items. Shape out of range: FMLP_ERR_SHAPE; a NULL pointer:
- * FMLP_ERR_NULL. */
+ * K steps of 64 per tile, `pairs` CTA pairs. First-stage items are u = band * num_n1 + j; down
+ * items follow, n1 + band * num_n2 + n. Writes start[0 .. pairs] (pair p runs
+ * item[start[p] .. start[p + 1])) and the items (at most 2048), and their count to *n_items.
+ * Shape out of range: FMLP_ERR_SHAPE; a NULL pointer: FMLP_ERR_NULL. */
 FMLP_API fmlp_status fmlp_test_two_stage_schedule(int num_m, int num_n1, int num_n2, int kb1,
-                                                  int kb2, int lists, int mc, uint16_t* start,
+                                                  int kb2, int pairs, uint16_t* start,
                                                   uint16_t* item, int64_t* n_items);
 
 /* Plan switch for the few-token block launch, process-wide. Under FMLP_PLAN_TC a GeGLU block

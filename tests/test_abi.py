@@ -266,10 +266,10 @@ def test_decode_crossover_is_pure_host(lib):
     finally:
         fm.fmlp_test_prefer_decode(0)
     assert fm.fmlp_test_prefer_decode(2, raise_on_error=False) == fm.FMLP_ERR_SHAPE
-    # the two-stage switch: -1, 0, 1, 2 accepted; the plan stays FMLP_PLAN_TC either way
-    for bad in (3, -2):
+    # the two-stage switch: -1, 0, 1 accepted; the plan stays FMLP_PLAN_TC either way
+    for bad in (2, -2):
         assert fm.fmlp_test_two_stage(bad, raise_on_error=False) == fm.FMLP_ERR_SHAPE
-    for mode in (-1, 2, 1, 0):
+    for mode in (-1, 1, 0):
         assert fm.fmlp_test_two_stage(mode) == fm.FMLP_OK
         assert fm.fmlp_geglu_plan(8192, 768, 3072) == fm.FMLP_PLAN_TC
     assert fm.fmlp_mlp_gelu_plan(5, 4096, 4096, 4096) == fm.FMLP_PLAN_TC

@@ -47,12 +47,10 @@ def _lib():
     assert fm.fmlp_device_status() == fm.FMLP_OK, fm.fmlp_last_error()
 
 
-@pytest.fixture(params=[1, 2], ids=["pair-lists", "multicast-pairs"])
-def two_stage(request):
-    """Forced two-stage launches: one item list per CTA pair, or (2) one per cluster of two
-    pairs that share the x band (first stage) or the weight rows (down) through multicast."""
-    fm.fmlp_test_two_stage(request.param)
-    yield request.param
+@pytest.fixture
+def two_stage():
+    fm.fmlp_test_two_stage(1)
+    yield
     fm.fmlp_test_two_stage(0)
 
 
@@ -111,9 +109,8 @@ def test_mlp_two_stage_vs_oracle(T, D, H, Dout, mode, two_stage):
                   f"two-stage mlp {T}x{D}x{H}x{Dout}")
 
 
-@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T,D,H", [(1000, 512, 1032), (2048, 768, 3072), (777, 776, 2056)])
-def test_geglu_two_stage_bit_identical_to_two_launches(T, D, H, mode):
+def test_geglu_two_stage_bit_identical_to_two_launches(T, D, H):
     """Same 256-row tiles, same K order, same roundings: the one-launch and two-launch paths
     agree bit for bit under the CTA-pair tile policy."""
     ins = geglu_inputs(T, D, H)
@@ -122,7 +119,7 @@ def test_geglu_two_stage_bit_identical_to_two_launches(T, D, H, mode):
         fm.fmlp_test_two_stage(-1)
         assert ONE_LAUNCH not in fm.fmlp_describe_plan("geglu", T, D, H)
         y2 = run_geglu(ins, T, D, H)
-        fm.fmlp_test_two_stage(mode)
+        fm.fmlp_test_two_stage(1)
         assert ONE_LAUNCH in fm.fmlp_describe_plan("geglu", T, D, H)
         y1 = run_geglu(ins, T, D, H)
     finally:
@@ -131,29 +128,19 @@ def test_geglu_two_stage_bit_identical_to_two_launches(T, D, H, mode):
     assert np.array_equal(y1, y2)
 
 
-@pytest.mark.parametrize("mode", [1, 2])
-def test_mlp_two_stage_bit_identical_to_two_launches(mode):
+def test_mlp_two_stage_bit_identical_to_two_launches():
     T, D, H, Dout = 1000, 1024, 2048, 776
     ins = mlp_inputs(T, D, H, Dout)
     fm.fmlp_set_tile_policy(fm.FMLP_TILES_PAIR)
     try:
         fm.fmlp_test_two_stage(-1)
         y2 = run_mlp(ins, T, D, H, Dout, fm.FMLP_GELU_TANH)
-        fm.fmlp_test_two_stage(mode)
+        fm.fmlp_test_two_stage(1)
         y1 = run_mlp(ins, T, D, H, Dout, fm.FMLP_GELU_TANH)
     finally:
         fm.fmlp_test_two_stage(0)
         fm.fmlp_set_tile_policy(fm.FMLP_TILES_AUTO)
     assert np.array_equal(y1, y2)
-
-
-def test_multicast_pairs_describe_their_clusters():
-    fm.fmlp_test_two_stage(2)
-    try:
-        text = fm.fmlp_describe_plan("geglu", 2048, 768, 3072)
-    finally:
-        fm.fmlp_test_two_stage(0)
-    assert ONE_LAUNCH in text and "multicast" in text, text
 
 
 def test_two_stage_is_one_kernel(two_stage):
